@@ -1,0 +1,89 @@
+"""Low-bit MLA decode for GB300: Python binding of the C ABI in include/qmla.h.
+
+Every function below only marshals arguments (torch tensors -> device
+pointers, the current CUDA stream) and calls the function of the same name in
+libqmla.so; all computation runs in the library's CUDA kernels.  Errors
+returned by the library raise QmlaError.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+from . import _lib
+
+C4R4, C2R4, BF16 = 0, 1, 2
+FORMAT_NAMES = {"C4R4": C4R4, "C2R4": C2R4, "BF16": BF16}
+D_C, D_R, GROUP, BLOCK_TOKENS = 512, 64, 64, 64
+
+QMLA_OK = 0
+QMLA_STATUS_BAD_BLOCK, QMLA_STATUS_BAD_LEN, QMLA_STATUS_TIMEOUT = 0x1, 0x2, 0x4
+
+
+class QmlaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = _lib.load().qmla_error_string(code).decode()
+        super().__init__(f"{fn} failed: {msg} ({code})")
+        self.code = code
+
+
+def _fmt(f) -> int:
+    return FORMAT_NAMES[f] if isinstance(f, str) else int(f)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _p(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _check(fn: str, code: int) -> None:
+    if code != QMLA_OK:
+        raise QmlaError(fn, code)
+
+
+def qmla_block_bytes(fmt) -> int:
+    return int(_lib.load().qmla_block_bytes(_fmt(fmt)))
+
+
+def qmla_error_string(code: int) -> str:
+    return _lib.load().qmla_error_string(int(code)).decode()
+
+
+def qmla_append(fmt, blocks, block_table, positions, latent, rope_k, status,
+                stream=None) -> None:
+    """Quantize and pack latent [B][n_new][512] / rope_k [B][n_new][64] (bf16,
+    device) into the block pool ``blocks`` (uint8, device)."""
+    B, n_new = int(latent.shape[0]), int(latent.shape[1])
+    num_blocks = blocks.numel() // qmla_block_bytes(fmt)
+    code = _lib.load().qmla_append(
+        _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
+        _p(positions), B, n_new, _p(latent), _p(rope_k), _p(status), _stream(stream))
+    _check("qmla_append", code)
+
+
+def qmla_decode_workspace_bytes(fmt, batch: int, heads: int, max_seq_len: int) -> int:
+    return int(_lib.load().qmla_decode_workspace_bytes(_fmt(fmt), int(batch), int(heads),
+                                                       int(max_seq_len)))
+
+
+def qmla_decode(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r, scale: float,
+                out, lse, workspace, status, stream=None) -> None:
+    """Absorbed-query MLA decode; writes out [B][H][512] bf16 and lse [B][H] f32."""
+    B, H = int(q_c.shape[0]), int(q_c.shape[1])
+    num_blocks = blocks.numel() // qmla_block_bytes(fmt)
+    code = _lib.load().qmla_decode(
+        _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
+        _p(seq_lens), int(max_seq_len), B, H, _p(q_c), _p(q_r), float(scale), _p(out), _p(lse),
+        _p(workspace), int(workspace.numel() * workspace.element_size()), _p(status),
+        _stream(stream))
+    _check("qmla_decode", code)
+
+
+def qmla_read_status(status, stream=None) -> int:
+    """Synchronize the stream and return QMLA_OK or QMLA_ERR_DEVICE."""
+    return int(_lib.load().qmla_read_status(_p(status), _stream(stream)))
