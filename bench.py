@@ -1,0 +1,471 @@
+"""Benchmark of the low-bit MLA decode hot path (qmla_append + qmla_decode).
+
+One step = append one new token to every sequence (quantize + pack) and run
+one decode over the whole cache (split-KV attention + log-sum-exp merge).
+Default workload: C4R4 cache, 32 sequences of 8192 tokens, 16 heads.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..4]
+                  [--format C4R4|C2R4|BF16] [--impl ours|reference] [--no-also]
+
+Prints ONE JSON line on rank 0.  `value` is cached tokens attended per second
+(sum over the sequences of the tokens each decode attends, divided by the
+device time of the steps), aggregated over all ranks.  Inputs are synthetic
+and seeded (bit_mla_kv_qmla_gb300/workloads.py).  `--impl reference` times the
+CPU oracle on the host cores instead, on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "low-bit MLA decode: cached tokens attended/s and % of roofline at 1 GPU"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 2**20
+TOKEN_BYTES = {"C4R4": 324, "C2R4": 196, "BF16": 1152}
+FLOP_PER_TOKEN_HEAD = 2 * (576 + 512)
+IO_BYTES_PER_HEAD = 576 * 2 + 512 * 2 + 4  # q in, O out, LSE out
+DECODE_SOURCES = ["decode_tc.cu", "decode_simt.cu", "plan.cuh", "qmla_internal.cuh",
+                  "combine.cu"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def decode_kernel_hash():
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        p = os.path.join(ROOT, "bit_mla_kv_qmla_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was
+    taken on the current decode kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(workload_name)
+    if not ent or ent.get("kernel_hash") != decode_kernel_hash():
+        return None
+    return ent.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            import torch
+            ident = str(self.device_index)
+            try:
+                u = str(torch.cuda.get_device_properties(self.device_index).uuid)
+                ident = u if u.startswith("GPU-") else "GPU-" + u
+            except Exception:
+                pass
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", ident], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[4 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def roofline_for(fmt, heads, lens, t_s, pk, traffic):
+    tokens = sum(lens)
+    B = len(lens)
+    nbytes = tokens * TOKEN_BYTES[fmt] + B * heads * IO_BYTES_PER_HEAD
+    flops = tokens * heads * FLOP_PER_TOKEN_HEAD
+    t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    if t_mem >= t_tc:
+        ach = nbytes / t_s / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "algorithmic_bytes": nbytes, "peak_source": pk["source"]}
+    ach = flops / t_s / 1e12
+    return {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
+            "algorithmic_flops": flops, "peak_source": pk["source"],
+            "peak_note": "f16 operands: same nominal dense rate as bf16"}
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import bit_mla_kv_qmla_gb300 as q
+    from bit_mla_kv_qmla_gb300 import workloads as W
+    from bit_mla_kv_qmla_gb300.cache import Decoder, build_cache
+
+    w = W.with_format(W.WORKLOADS[args.config], args.format or W.WORKLOADS[args.config].fmt)
+    lens0 = W.seq_lens(w)
+    n_app = max(1, w.n_append) if args.config == 1 else w.n_append
+    total_steps = args.steps + args.warmup
+    extra = n_app * (total_steps + 2 * args.e2e_steps + 4)
+    cache_bytes = sum(W.blocks_needed(lens0, extra)) * q.qmla_block_bytes(w.fmt)
+    copies = 1 if cache_bytes >= 2 * L2_BYTES else max(2, math.ceil(2 * L2_BYTES / cache_bytes))
+    caches = [build_cache(w, device, extra_tokens=extra) for _ in range(copies)]
+    max_len = max(lens0) + extra
+    decs = [Decoder(c, w.heads, max_len) for c in caches]
+    qc, qr = W.queries(w, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(1234 + rank)
+    new_lat = torch.randn(copies, w.batch, max(n_app, 1), 512, generator=g, device=device)
+    new_rope = torch.randn(copies, w.batch, max(n_app, 1), 64, generator=g, device=device)
+    new_lat, new_rope = new_lat.to(torch.bfloat16), new_rope.to(torch.bfloat16)
+    stream = torch.cuda.current_stream(device)
+    torch.cuda.synchronize(device)
+    for c in caches:
+        assert c.status.item() == 0
+
+    def step(k):
+        i = k % copies
+        if n_app:
+            caches[i].append(new_lat[i, :, :n_app], new_rope[i, :, :n_app])
+        decs[i](qc, qr, w.scale)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize(device)
+    lens_at = [list(c.seq_lens.cpu().tolist()) for c in caches]
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.15)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    tokens = 0
+    t0.record(stream)
+    for k in range(args.warmup, total_steps):
+        i = k % copies
+        if n_app:
+            caches[i].append(new_lat[i, :, :n_app], new_rope[i, :, :n_app])
+            lens_at[i] = [L + n_app for L in lens_at[i]]
+        e = ev[k - args.warmup]
+        e[0].record(stream)
+        decs[i](qc, qr, w.scale)
+        e[1].record(stream)
+        tokens += sum(lens_at[i])
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    t_dec = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
+    for c in caches:
+        assert c.status.item() == 0, "device status flag set during the benchmark"
+
+    # end to end through the public API with host buffers: per step, pinned
+    # host -> device copy of the step's inputs (new tokens, queries), the two
+    # library calls, device -> host read of O and LSE.
+    e2e = None
+    if args.e2e_steps > 0:
+        h_lat = new_lat[0, :, :max(n_app, 1)].cpu().pin_memory()
+        h_rope = new_rope[0, :, :max(n_app, 1)].cpu().pin_memory()
+        h_qc, h_qr = qc.cpu().pin_memory(), qr.cpu().pin_memory()
+        d_lat, d_rope = torch.empty_like(new_lat[0, :, :max(n_app, 1)]), torch.empty_like(
+            new_rope[0, :, :max(n_app, 1)])
+        d_qc, d_qr = torch.empty_like(qc), torch.empty_like(qr)
+        h_out = torch.empty(decs[0].out.shape, dtype=torch.bfloat16).pin_memory()
+        h_lse = torch.empty(decs[0].lse.shape, dtype=torch.float32).pin_memory()
+        h2d = (h_lat.numel() * 2 + h_rope.numel() * 2 if n_app else 0) + h_qc.numel() * 2 + \
+            h_qr.numel() * 2
+        d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+        def e2e_step(i):
+            if n_app:
+                d_lat.copy_(h_lat, non_blocking=True)
+                d_rope.copy_(h_rope, non_blocking=True)
+                caches[i].append(d_lat[:, :n_app], d_rope[:, :n_app])
+            d_qc.copy_(h_qc, non_blocking=True)
+            d_qr.copy_(h_qr, non_blocking=True)
+            out, lse = decs[i](d_qc, d_qr, w.scale)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            torch.cuda.current_stream(device).synchronize()
+
+        for k in range(3):
+            e2e_step(k % copies)
+        tok_e2e = 0
+        s0 = time.perf_counter()
+        for k in range(args.e2e_steps):
+            i = k % copies
+            e2e_step(i)
+            lens_at[i] = [L + n_app for L in lens_at[i]]
+            tok_e2e += sum(lens_at[i])
+        e2e_t = time.perf_counter() - s0
+        e2e = {"value": tok_e2e / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "ms_per_step": 1e3 * e2e_t / args.e2e_steps}
+
+    lens_mid = [L for L in lens_at[0]]
+    pk = peaks()
+    roof = roofline_for(w.fmt, w.heads, lens_mid, t_dec, pk, recorded_traffic(w.name))
+    roof["kernel"] = "qmla_decode (split-KV decode + combine), CUDA events per call"
+    roof["decode_ms"] = round(t_dec * 1e3, 5)
+    res = {"tokens": tokens, "elapsed": elapsed, "t_dec": t_dec, "roofline": roof,
+           "clocks": clocks, "e2e": e2e, "workload": w, "copies": copies,
+           "cache_bytes": cache_bytes, "launches": args.steps * ((1 if n_app else 0) + 2)}
+    return res
+
+
+def measure_also(args, device):
+    """Device-timed decode of the other workloads (no append), for context."""
+    import torch
+    from bit_mla_kv_qmla_gb300 import workloads as W
+    from bit_mla_kv_qmla_gb300.cache import Decoder, build_cache
+    out = {}
+    pk = peaks()
+    for cfg, fmt in [(4, "C4R4"), (4, "C2R4"), (4, "BF16"), (2, "C4R4"), (3, "C2R4")]:
+        w = W.with_format(W.WORKLOADS[cfg], fmt)
+        lens = W.seq_lens(w)
+        cache = build_cache(w, device)
+        dec = Decoder(cache, w.heads, max(lens))
+        qc, qr = W.queries(w, device=device)
+        for _ in range(3):
+            dec(qc, qr, w.scale)
+        torch.cuda.synchronize(device)
+        n = 10
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        for a, b in evs:
+            flush.fill_(1.0)  # evict the cache from L2 between calls (untimed)
+            a.record()
+            dec(qc, qr, w.scale)
+            b.record()
+        torch.cuda.synchronize(device)
+        assert cache.status.item() == 0
+        t = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+        roof = roofline_for(fmt, w.heads, lens, t, pk, recorded_traffic(w.name))
+        out[w.name] = {"tokens_per_s": sum(lens) / t, "decode_us": round(t * 1e6, 2),
+                       "roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "frac")},
+                       "cache_bytes": cache.blocks.numel()}
+        del cache, dec, flush
+        torch.cuda.empty_cache()
+    return out
+
+
+def footprint_sweep():
+    """Max concurrent L=131072 sequences in a 150 GB (1e9 B) cache budget."""
+    import bit_mla_kv_qmla_gb300 as q
+    budget = 150e9
+    per_seq = {f: (131072 // 64) * q.qmla_block_bytes(f) for f in ("BF16", "C4R4", "C2R4")}
+    mx = {f: int(budget // per_seq[f]) for f in per_seq}
+    return {"budget_bytes": int(budget), "seq_len": 131072, "bytes_per_seq": per_seq,
+            "max_sequences": mx,
+            "gain_vs_bf16": {f: round(mx[f] / mx["BF16"], 3) for f in mx}}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (reference and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+class OracleRunner:
+    """The oracle's step (append one token to each sampled sequence, then
+    decode them with every head), on the host, single-threaded."""
+
+    def __init__(self, cfg, fmt, n_seq, max_steps):
+        import numpy as np
+        import oracle
+        from bit_mla_kv_qmla_gb300 import workloads as W
+        self.np, self.oracle, self.W = np, oracle, W
+        self.w = w = W.with_format(W.WORKLOADS[cfg], fmt)
+        self.n_seq = n_seq
+        lens = W.seq_lens(w)[:n_seq]
+        self.f = W.FORMATS[w.fmt]
+        need = [(L + max_steps + 1 + 63) // 64 for L in lens]
+        self.table = np.full((n_seq, max(need)), -1, np.int32)
+        k = 0
+        for b, n in enumerate(need):
+            self.table[b, :n] = np.arange(k, k + n)
+            k += n
+        self.pool = np.zeros(k * oracle.block_bytes(self.f), np.uint8)
+        for b, L in enumerate(lens):
+            lat, rope = W.tokens(w, b, L)
+            oracle.append(self.f, self.pool, self.table[b:b + 1], np.array([0], np.int32),
+                          lat[None], rope[None])
+        qc, qr = W.queries(w)
+        self.qc, self.qr = qc[:n_seq], qr[:n_seq]
+        self.cur = np.array(lens, np.int32)
+        self.s = 0
+        self.sample = f"{n_seq} of {w.batch} sequences x {w.heads} heads per step"
+
+    def step(self):
+        self.s += 1
+        lat, rope = self.W.tokens(self.w, 0, self.n_seq, offset_seed=self.s)
+        self.oracle.append(self.f, self.pool, self.table, self.cur, lat[:, None], rope[:, None])
+        self.cur = self.cur + 1
+        self.oracle.decode(self.f, self.pool, self.table, self.cur, self.qc, self.qr, self.w.scale)
+        return int(self.cur.sum())
+
+
+def cpu_baseline(cfg, fmt):
+    """The oracle timed on a bounded sample (about 10 s of host work)."""
+    r = OracleRunner(cfg, fmt, n_seq=8 if cfg == 1 else 1, max_steps=64)
+    tokens, t0 = 0, time.perf_counter()
+    steps = 0
+    while steps < 64 and (time.perf_counter() - t0 < 10.0 or steps < 1):
+        tokens += r.step()
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{r.sample}, {steps} step(s), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    ap.add_argument("--format", default=None, choices=["C4R4", "C2R4", "BF16"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from bit_mla_kv_qmla_gb300 import workloads as W
+        w = W.with_format(W.WORKLOADS[args.config], args.format or W.WORKLOADS[args.config].fmt)
+        r = OracleRunner(args.config, w.fmt, n_seq=2 if args.config == 1 else 1,
+                         max_steps=args.steps + args.warmup)
+        for _ in range(args.warmup):
+            r.step()
+        tokens, t0 = 0, time.perf_counter()
+        for _ in range(args.steps):
+            tokens += r.step()
+        t_all = time.perf_counter() - t0
+        v = tokens / t_all
+        sample = r.sample
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "format": w.fmt, "batch": w.batch,
+                           "heads": w.heads, "seq_len": w.seq_len},
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    res = run_ours(args, rank, world, device)
+    tok, el = float(res["tokens"]), float(res["elapsed"])
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([el], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        n = torch.tensor([tok], dtype=torch.float64, device=device)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        el, tok = float(t.item()), float(n.item())
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    w = res["workload"]
+    also = None if args.no_also or world > 1 else measure_also(args, device)
+    line = {
+        "metric": METRIC, "value": tok / el, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded, bit_mla_kv_qmla_gb300/workloads.py)",
+        "config": {"workload": w.name, "format": w.fmt, "batch": w.batch, "heads": w.heads,
+                   "seq_len": w.seq_len, "append_per_step": max(1, w.n_append),
+                   "l2": (f"rotating {res['copies']} cache copies of "
+                          f"{res['cache_bytes'] / 1e6:.0f} MB (> L2 129 MB in total)"
+                          if res["copies"] > 1 else "cache larger than L2")},
+        "roofline": res["roofline"],
+        "cpu_baseline": None if args.no_cpu_baseline else cpu_baseline(args.config, w.fmt),
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "footprint_150GB": footprint_sweep(),
+        "also": also,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+// append.cu - quantize-and-pack of new tokens into the paged low-bit cache.
+//
+// The two quantizers of "QuantMLA: INT4 (and INT2) for both halves of the MLA
+// cache" (flowchart: content quant INT4 or INT2, RoPE quant INT4): each token's
+// 512-channel content latent and 64-channel RoPE key are cut into 64-channel
+// groups, each stored as binary16 (scale, zero) plus packed integer codes.
+// The rounding rules (zero rounded down, scale rounded up, codes rounded half
+// to even) are the ones specified in qmla.h; every step uses an explicitly
+// rounded intrinsic, so the result is bit-exact and independent of
+// compiler contraction.
+//
+// One CTA per new token, one warp per 64-channel group (8 content + 1 RoPE),
+// each lane holding two consecutive channels.  The whole append is one pass
+// over the new tokens: it is launch-bound for decode-sized appends.
+
+#include "qmla_internal.cuh"
+
+namespace qmla {
+namespace {
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Quantize the warp's group; lane holds channels 2*lane and 2*lane+1 (x0, x1).
+// Returns the two codes and (scale, zero) as binary16 bits.
+__device__ __forceinline__ void quantize_pair(float x0, float x1, int bits, uint32_t& c0,
+                                              uint32_t& c1, uint16_t& s_bits,
+                                              uint16_t& z_bits) {
+  const float mn = warp_min(fminf(x0, x1));
+  const float mx = warp_max(fmaxf(x0, x1));
+  const __half z = __float2half_rd(mn);
+  const float zf = __half2float(z);
+  const float r = __fsub_ru(mx, zf);
+  z_bits = __half_as_ushort(z);
+  if (r == 0.0f) {
+    s_bits = 0;
+    c0 = c1 = 0;
+    return;
+  }
+  const float levels = float((1 << bits) - 1);
+  const __half s = __float2half_ru(__fdiv_ru(r, levels));
+  const float sf = __half2float(s);
+  s_bits = __half_as_ushort(s);
+  const float t0 = rintf(__fdiv_rn(__fsub_rn(x0, zf), sf));
+  const float t1 = rintf(__fdiv_rn(__fsub_rn(x1, zf), sf));
+  c0 = uint32_t(fminf(fmaxf(t0, 0.0f), levels));
+  c1 = uint32_t(fminf(fmaxf(t1, 0.0f), levels));
+}
+
+// Pack: the lane's even channel goes to position j of the low half-word, its
+// odd channel to position j of the high half-word, j = lane % (codes per
+// half-word); OR-reduce across the lanes sharing a word.
+__device__ __forceinline__ uint32_t pack_word(uint32_t c0, uint32_t c1, int bits, int lane) {
+  const int per_half = 16 / bits;  // 4 (INT4) or 8 (INT2) lanes share a word
+  const int j = lane % per_half;
+  uint32_t w = (c0 << (bits * j)) | (c1 << (16 + bits * j));
+  for (int o = 1; o < per_half; o <<= 1) w |= __shfl_xor_sync(0xffffffffu, w, o);
+  return w;
+}
+
+__global__ void __launch_bounds__(288) append_kernel(
+    int fmt, uint8_t* __restrict__ blocks, int64_t num_blocks, const int32_t* __restrict__ table,
+    int max_blocks, const int32_t* __restrict__ positions, int n_new,
+    const __nv_bfloat16* __restrict__ latent, const __nv_bfloat16* __restrict__ rope,
+    int32_t* status) {
+  const int tok = blockIdx.x;  // b * n_new + i
+  const int b = tok / n_new, i = tok % n_new;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t pos = int64_t(positions[b]) + i;
+  const int64_t jb = pos / kT;
+  if (pos < 0 || jb >= max_blocks) {
+    if (threadIdx.x == 0) set_status(status, QMLA_STATUS_BAD_LEN);
+    return;
+  }
+  const int32_t blk_id = table[int64_t(b) * max_blocks + jb];
+  if (blk_id < 0 || blk_id >= num_blocks) {
+    if (threadIdx.x == 0) set_status(status, QMLA_STATUS_BAD_BLOCK);
+    return;
+  }
+  const Geom G = geom(fmt);
+  const int slot = int(pos % kT);
+  uint8_t* blk = blocks + int64_t(blk_id) * G.block;
+
+  // the lane's two channels of this warp's group
+  __nv_bfloat162 v;
+  if (warp < 8) {
+    v = reinterpret_cast<const __nv_bfloat162*>(latent + int64_t(tok) * kDc + warp * kG)[lane];
+  } else {
+    v = reinterpret_cast<const __nv_bfloat162*>(rope + int64_t(tok) * kDr)[lane];
+  }
+
+  if (fmt == QMLA_BF16) {
+    uint8_t* dst;
+    if (warp < 8) {
+      const int h = warp / 4, gi = warp % 4;
+      dst = blk + h * G.half + G.content_off + (gi * kT + slot) * 128 + lane * 4;
+    } else {
+      const int h = lane / 16;  // lane holds RoPE channels 2*lane, 2*lane+1
+      dst = blk + h * G.half + G.rope_off + slot * 64 + (lane % 16) * 4;
+    }
+    *reinterpret_cast<__nv_bfloat162*>(dst) = v;
+    return;
+  }
+
+  const float x0 = __bfloat162float(v.x), x1 = __bfloat162float(v.y);
+  const int bits = (warp < 8) ? G.cbits : 4;
+  uint32_t c0, c1;
+  uint16_t s_bits, z_bits;
+  quantize_pair(x0, x1, bits, c0, c1, s_bits, z_bits);
+  const uint32_t word = pack_word(c0, c1, bits, lane);
+  const int per_word_lanes = 16 / bits;  // lanes per 32-bit word
+  const int w = lane / per_word_lanes;
+  const uint32_t sz = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
+  if (warp < 8) {
+    const int h = warp / 4, gi = warp % 4;
+    uint8_t* half = blk + h * G.half;
+    if (lane % per_word_lanes == 0)
+      reinterpret_cast<uint32_t*>(half + G.content_off + (gi * kT + slot) * G.code_bytes)[w] = word;
+    if (lane == 0) reinterpret_cast<uint32_t*>(half + G.sz_off + (gi * kT + slot) * 4)[0] = sz;
+  } else {
+    // RoPE: 8 words of 8 channels; words 0-3 -> half 0, words 4-7 -> half 1
+    if (lane % 4 == 0) {
+      const int h = w / 4;
+      reinterpret_cast<uint32_t*>(blk + h * G.half + G.rope_off + slot * 16)[w % 4] = word;
+    }
+    if (lane == 0) reinterpret_cast<uint32_t*>(blk + G.rope_sz_off + slot * 4)[0] = sz;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(int fmt, uint8_t* blocks, int64_t num_blocks, const int32_t* table,
+                          int max_blocks, const int32_t* positions, int batch, int n_new,
+                          const __nv_bfloat16* latent, const __nv_bfloat16* rope,
+                          int32_t* status, cudaStream_t stream) {
+  const int64_t ntok = int64_t(batch) * n_new;
+  if (ntok == 0) return cudaSuccess;
+  append_kernel<<<dim3(unsigned(ntok)), 288, 0, stream>>>(fmt, blocks, num_blocks, table,
+                                                         max_blocks, positions, n_new, latent,
+                                                         rope, status);
+  return cudaGetLastError();
+}
+
+}  // namespace qmla

@@ -1,0 +1,55 @@
+// combine.cu - log-sum-exp merge of the split-KV partials.
+//
+// Each piece i of a sequence holds a normalized partial O_i and its LSE_i;
+// the full result is LSE = ln sum_i exp(LSE_i) and
+// O = sum_i exp(LSE_i - LSE) * O_i, written as bfloat16 O and binary32 LSE.
+// A sequence with no piece (length 0) gets O = 0 and LSE = -inf.
+// Grid (batch, heads), 128 threads, 4 channels per thread.
+
+#include <cfloat>
+
+#include "qmla_internal.cuh"
+
+namespace qmla {
+namespace {
+
+__global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int heads,
+                                                      __nv_bfloat16* __restrict__ out,
+                                                      float* __restrict__ lse) {
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int2 ent = ws.seq_table[b];
+  const int base = ent.x, n = ent.y;
+  float m = -INFINITY;
+  for (int i = 0; i < n; ++i) m = fmaxf(m, ws.part_lse[int64_t(base + i) * heads + h]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = -INFINITY;
+  if (m > -INFINITY) {
+    float sum = 0.0f;
+    for (int i = 0; i < n; ++i) sum += __expf(ws.part_lse[int64_t(base + i) * heads + h] - m);
+    L = m + logf(sum);
+    for (int i = 0; i < n; ++i) {
+      const float wgt = __expf(ws.part_lse[int64_t(base + i) * heads + h] - L);
+      const float4 o = reinterpret_cast<const float4*>(
+          ws.part_o + (int64_t(base + i) * heads + h) * kDc)[tid];
+      acc.x = fmaf(wgt, o.x, acc.x);
+      acc.y = fmaf(wgt, o.y, acc.y);
+      acc.z = fmaf(wgt, o.z, acc.z);
+      acc.w = fmaf(wgt, o.w, acc.w);
+    }
+  }
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + (int64_t(b) * heads + h) * kDc) + 2 * tid;
+  dst[0] = __floats2bfloat162_rn(acc.x, acc.y);
+  dst[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  if (tid == 0) lse[int64_t(b) * heads + h] = L;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Workspace& ws, int batch, int heads, __nv_bfloat16* out,
+                           float* lse, cudaStream_t stream) {
+  if (batch == 0) return cudaSuccess;
+  combine_kernel<<<dim3(unsigned(batch), unsigned(heads)), 128, 0, stream>>>(ws, heads, out, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace qmla

@@ -1,0 +1,148 @@
+// qmla_api.cu - the exported C ABI (declared and documented in qmla.h).
+//
+// Host code only: argument validation, choice of kernel, split planning
+// constants and launches on the caller's stream.  No allocation, no global
+// state beyond what the CUDA runtime keeps per function.
+
+#include <cstdio>
+
+#include "qmla_internal.cuh"
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool known_format(int f) { return f == QMLA_C4R4 || f == QMLA_C2R4 || f == QMLA_BF16; }
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+bool heads_served(int fmt, int heads) {
+  return qmla::tc_supported(fmt, heads) || (heads > 0 && heads <= 256 && heads % 16 == 0);
+}
+
+// Partial slots a decode can need: one per sequence plus one per worker
+// boundary that falls inside a sequence.
+int max_slots(int batch, int heads, int sms) {
+  const int w = qmla::simt_workers(sms) > qmla::tc_workers(sms, heads)
+                    ? qmla::simt_workers(sms) : qmla::tc_workers(sms, heads);
+  return batch + w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qmla_block_bytes(int format) {
+  if (!known_format(format)) return 0;
+  return size_t(qmla::geom(format).block);
+}
+
+const char* qmla_error_string(int code) {
+  switch (code) {
+    case QMLA_OK: return "ok";
+    case QMLA_ERR_INVALID_ARG: return "invalid argument";
+    case QMLA_ERR_UNSUPPORTED: return "unsupported format or shape";
+    case QMLA_ERR_CAPACITY: return "request exceeds a fixed capacity";
+    case QMLA_ERR_WORKSPACE: return "workspace too small";
+    case QMLA_ERR_CUDA: return "CUDA runtime error";
+    case QMLA_ERR_DEVICE: return "device status flag set";
+    default: return "unknown error";
+  }
+}
+
+int qmla_append(int format, void* blocks, int64_t num_blocks, const int32_t* block_table,
+                int32_t max_blocks_per_seq, const int32_t* positions, int32_t batch, int32_t n_new,
+                const void* latent, const void* rope_k, int32_t* status_dev, void* stream) {
+  if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
+  if (batch < 0 || n_new < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
+    return QMLA_ERR_INVALID_ARG;
+  if (int64_t(batch) * n_new == 0) return QMLA_OK;
+  if (int64_t(batch) * n_new > 0x7fffffffLL) return QMLA_ERR_CAPACITY;
+  if (!blocks || !block_table || !positions || !latent || !rope_k || !status_dev)
+    return QMLA_ERR_INVALID_ARG;
+  if (!aligned(blocks, 256) || !aligned(latent, 4) || !aligned(rope_k, 4) ||
+      !aligned(block_table, 4) || !aligned(positions, 4) || !aligned(status_dev, 4))
+    return QMLA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq == 0) return QMLA_ERR_INVALID_ARG;
+  cudaError_t e = qmla::launch_append(
+      format, static_cast<uint8_t*>(blocks), num_blocks, block_table, max_blocks_per_seq,
+      positions, batch, n_new, static_cast<const __nv_bfloat16*>(latent),
+      static_cast<const __nv_bfloat16*>(rope_k), status_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
+}
+
+size_t qmla_decode_workspace_bytes(int format, int32_t batch, int32_t heads, int32_t max_seq_len) {
+  if (!known_format(format) || batch < 0 || max_seq_len < 0 || !heads_served(format, heads))
+    return 0;
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  return qmla::workspace_bytes(batch, heads, max_slots(batch, heads, sms));
+}
+
+int qmla_decode(int format, const void* blocks, int64_t num_blocks, const int32_t* block_table,
+                int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                int32_t batch, int32_t heads, const void* q_c, const void* q_r,
+                float softmax_scale, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
+  if (batch < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
+    return QMLA_ERR_INVALID_ARG;
+  if (!heads_served(format, heads)) return QMLA_ERR_UNSUPPORTED;
+  if (batch == 0) return QMLA_OK;
+  if (!blocks || !block_table || !seq_lens || !q_c || !q_r || !out || !lse || !workspace ||
+      !status_dev)
+    return QMLA_ERR_INVALID_ARG;
+  if (!aligned(blocks, 256) || !aligned(workspace, 256) || !aligned(q_c, 16) ||
+      !aligned(q_r, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(seq_lens, 4) ||
+      !aligned(block_table, 4) || !aligned(status_dev, 4))
+    return QMLA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq == 0) return QMLA_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return QMLA_ERR_CUDA;
+  const int slots = max_slots(batch, heads, sms);
+  if (workspace_bytes < qmla::workspace_bytes(batch, heads, slots)) return QMLA_ERR_WORKSPACE;
+
+  qmla::DecodeArgs a;
+  a.fmt = format;
+  a.blocks = static_cast<const uint8_t*>(blocks);
+  a.num_blocks = num_blocks;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.seq_lens = seq_lens;
+  a.max_seq_len = max_seq_len;
+  a.batch = batch;
+  a.heads = heads;
+  a.q_c = static_cast<const __nv_bfloat16*>(q_c);
+  a.q_r = static_cast<const __nv_bfloat16*>(q_r);
+  a.scale = softmax_scale;
+  a.ws = qmla::carve(workspace, batch, heads, slots);
+  a.status = status_dev;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (qmla::tc_supported(format, heads)) {
+    a.workers = qmla::tc_workers(sms, heads);
+    e = qmla::launch_decode_tc(a, s);
+  } else {
+    a.workers = qmla::simt_workers(sms);
+    e = qmla::launch_decode_simt(a, s);
+  }
+  if (e != cudaSuccess) return QMLA_ERR_CUDA;
+  e = qmla::launch_combine(a.ws, batch, heads, static_cast<__nv_bfloat16*>(out), lse, s);
+  return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
+}
+
+int qmla_read_status(const int32_t* status_dev, void* stream) {
+  if (!status_dev) return QMLA_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, status_dev, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return QMLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QMLA_ERR_CUDA;
+  return v == 0 ? QMLA_OK : QMLA_ERR_DEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// qmla_internal.cuh - layout constants and shared device helpers of the CUDA
+// path.  The byte layout implemented here is the one specified in qmla.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "qmla.h"
+
+namespace qmla {
+
+constexpr int kDc = QMLA_D_C;
+constexpr int kDr = QMLA_D_R;
+constexpr int kG = QMLA_GROUP;
+constexpr int kT = QMLA_BLOCK_TOKENS;
+
+// Per-format byte geometry of a 64-token block.
+struct Geom {
+  int fmt;
+  int cbits;        // content code bits (4, 2; 16 = bf16)
+  int code_bytes;   // bytes of one content group of one token (32, 16, 128)
+  int half;         // bytes of one half-block
+  int content_off;  // offset of content codes inside a half (0)
+  int rope_off;     // offset of RoPE codes inside a half
+  int sz_off;       // offset of content scale/zero inside a half
+  int rope_sz_off;  // offset of the shared RoPE scale/zero inside the block
+  int block;        // bytes of a block
+};
+
+__host__ __device__ constexpr Geom geom(int fmt) {
+  return fmt == QMLA_C4R4 ? Geom{QMLA_C4R4, 4, 32, 10240, 0, 8192, 9216, 20480, 20736}
+       : fmt == QMLA_C2R4 ? Geom{QMLA_C2R4, 2, 16, 6144, 0, 4096, 5120, 12288, 12544}
+                          : Geom{QMLA_BF16, 16, 128, 36864, 0, 32768, -1, -1, 73728};
+}
+
+// Device status word: OR in a bit (relaxed; read by the host after a sync).
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Number of 64-token blocks of a sequence of length L.
+__host__ __device__ __forceinline__ int blocks_of(int L) { return (L + kT - 1) / kT; }
+
+// Split plan.  The blocks of all sequences, concatenated in sequence order,
+// are cut into P contiguous ranges of near-equal size, one per worker (CTA or
+// CTA pair).  Worker w owns global blocks [start(w), start(w+1)) with
+// start(w) = floor(w*N/P).  A worker range that touches k sequences produces
+// k partial results ("pieces").  Pieces of sequence b get consecutive slots
+// base_b .. base_b + n_b - 1 of the partial buffers.
+__host__ __device__ __forceinline__ int64_t plan_start(int64_t w, int64_t N, int64_t P) {
+  return (w * N) / P;
+}
+// Worker owning global block g (0 <= g < N).
+__host__ __device__ __forceinline__ int64_t plan_owner(int64_t g, int64_t N, int64_t P) {
+  return ((g + 1) * P - 1) / N;
+}
+
+// Workspace layout for the decode: [seq table B x int2][part LSE slots x H]
+// [part O slots x H x 512] (each region 256-byte aligned).
+struct Workspace {
+  int2* seq_table;  // (first slot, number of pieces) per sequence
+  float* part_lse;
+  float* part_o;
+};
+__host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ __forceinline__ size_t workspace_bytes(int batch, int heads, int slots) {
+  return align256(size_t(batch) * sizeof(int2)) + align256(size_t(slots) * heads * sizeof(float)) +
+         align256(size_t(slots) * heads * kDc * sizeof(float));
+}
+__host__ __device__ __forceinline__ Workspace carve(void* ws, int batch, int heads, int slots) {
+  char* p = static_cast<char*>(ws);
+  Workspace w;
+  w.seq_table = reinterpret_cast<int2*>(p);
+  p += align256(size_t(batch) * sizeof(int2));
+  w.part_lse = reinterpret_cast<float*>(p);
+  p += align256(size_t(slots) * heads * sizeof(float));
+  w.part_o = reinterpret_cast<float*>(p);
+  return w;
+}
+
+// Arguments shared by the decode kernels.
+struct DecodeArgs {
+  int fmt;
+  const uint8_t* blocks;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int max_blocks_per_seq;
+  const int32_t* seq_lens;
+  int max_seq_len;
+  int batch;
+  int heads;
+  const __nv_bfloat16* q_c;
+  const __nv_bfloat16* q_r;
+  float scale;
+  Workspace ws;
+  int workers;  // P
+  int32_t* status;
+};
+
+// Kernel launchers (each defined next to its kernel).  They return a
+// cudaError_t from the launch.
+cudaError_t launch_append(int fmt, uint8_t* blocks, int64_t num_blocks, const int32_t* table,
+                          int max_blocks, const int32_t* positions, int batch, int n_new,
+                          const __nv_bfloat16* latent, const __nv_bfloat16* rope,
+                          int32_t* status, cudaStream_t stream);
+int simt_workers(int sms);
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
+int tc_workers(int sms, int heads);
+bool tc_supported(int fmt, int heads);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const Workspace& ws, int batch, int heads, __nv_bfloat16* out,
+                           float* lse, cudaStream_t stream);
+
+}  // namespace qmla

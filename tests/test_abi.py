@@ -1,0 +1,103 @@
+"""Host-side checks of the C-ABI library (no GPU needed, nothing launched).
+
+The library must load, export every function include/qmla.h declares, and
+reject bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_mla_kv_qmla_gb300 import build as B
+    B.build()
+    from bit_mla_kv_qmla_gb300 import _lib
+    return _lib.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(qmla_[a-z_0-9]+)\s*\(", src, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert names == sorted(["qmla_block_bytes", "qmla_append", "qmla_decode_workspace_bytes",
+                            "qmla_decode", "qmla_read_status", "qmla_error_string"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    # and nothing that looks like the oracle
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    assert "oracle" not in out
+
+
+def test_block_bytes(lib):
+    assert [lib.qmla_block_bytes(f) for f in (0, 1, 2, 3, -1)] == [20736, 12544, 73728, 0, 0]
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -99):
+        assert lib.qmla_error_string(code)
+
+
+P = ctypes.c_void_p
+
+
+def _fake(n):
+    # aligned host buffer used only as a non-null pointer value; never dereferenced
+    buf = ctypes.create_string_buffer(n + 512)
+    addr = (ctypes.addressof(buf) + 511) // 512 * 512
+    return buf, addr
+
+
+def test_append_rejects_bad_arguments(lib):
+    keep, p = _fake(1024)
+    ok_args = dict(format=0, blocks=p, num_blocks=4, table=p, maxb=2, pos=p, batch=1, n_new=1,
+                   lat=p, rope=p, status=p, stream=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.qmla_append(a["format"], a["blocks"], a["num_blocks"], a["table"], a["maxb"],
+                               a["pos"], a["batch"], a["n_new"], a["lat"], a["rope"], a["status"],
+                               a["stream"])
+    assert call(format=7) == -2
+    assert call(batch=-1) == -1
+    assert call(n_new=-1) == -1
+    assert call(num_blocks=0) == -1
+    assert call(blocks=None) == -1
+    assert call(lat=None) == -1
+    assert call(status=None) == -1
+    assert call(blocks=p + 16) == -1  # pool must be 256-byte aligned
+    assert call(maxb=0) == -1
+    assert call(batch=0) == 0  # nothing to do, nothing launched
+
+
+def test_decode_rejects_bad_arguments(lib):
+    keep, p = _fake(4096)
+
+    def call(fmt=0, heads=16, batch=1, blocks=p, ws=p, qc=p, out=p, wsb=1 << 20, maxb=4):
+        return lib.qmla_decode(fmt, blocks, 4, p, maxb, p, 256, batch, heads, qc, p,
+                               ctypes.c_float(0.1), out, p, ws, wsb, p, None)
+    assert call(fmt=5) == -2
+    assert call(heads=17) == -2
+    assert call(heads=512) == -2
+    assert call(batch=-1) == -1
+    assert call(blocks=None) == -1
+    assert call(qc=p + 8) == -1      # queries must be 16-byte aligned
+    assert call(ws=p + 128) == -1    # workspace must be 256-byte aligned
+    assert call(maxb=0) == -1
+    assert call(batch=0) == 0
+
+
+def test_read_status_null(lib):
+    assert lib.qmla_read_status(None, None) == -1

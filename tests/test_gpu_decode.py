@@ -1,0 +1,131 @@
+"""GPU parity of qmla_decode against the oracle.
+
+Small cases are compared in full (several blocks, ragged tails, empty
+sequences, every format and the served head counts); the full-size workloads
+are built on the GPU and compared on sampled (sequence, head) rows, with the
+oracle building its own cache from the same seeded tokens."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_mla_kv_qmla_gb300 import QMLA_STATUS_BAD_BLOCK, QMLA_STATUS_BAD_LEN
+from bit_mla_kv_qmla_gb300 import workloads as W
+from bit_mla_kv_qmla_gb300.cache import Decoder, PagedCache, build_cache
+
+from helpers import compare_rows, oracle_pool_for_seq, sample_heads
+
+pytestmark = pytest.mark.gpu
+FMTS = ["C4R4", "C2R4", "BF16"]
+
+
+def _small_workload(fmt, heads, seed):
+    return W.Workload(f"small_{fmt}_{heads}", fmt, 5, heads, 1000, 0, "lognormal8", 0, seed)
+
+
+def _oracle_full(w, cache, lens, qc, qr, gen_device):
+    table = cache.block_table.cpu().numpy()
+    refs_o, refs_l = [], []
+    for b, L in enumerate(lens):
+        pool = oracle_pool_for_seq(w, b, L, table[b], cache.num_blocks, gen_device)
+        o, l = oracle.decode(W.FORMATS[w.fmt], pool, table[b:b + 1], np.array([L]),
+                             qc[b:b + 1].cpu(), qr[b:b + 1].cpu(), w.scale)
+        refs_o.append(o[0])
+        refs_l.append(l[0])
+    return np.stack(refs_o), np.stack(refs_l)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("heads", [16, 32, 128])
+def test_decode_small_ragged(fmt, heads):
+    w = _small_workload(fmt, heads, 11)
+    lens = [1, 63, 65, 1000, 0]  # one token, partial block, block + 1, many blocks, empty
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cpu")
+    qc, qr = W.queries(w)
+    dec = Decoder(cache, heads, max(lens))
+    out, lse = dec(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    ref_o, ref_l = _oracle_full(w, cache, lens, qc, qr, "cpu")
+    compare_rows(out, lse, ref_o, ref_l, f"{fmt} H{heads}")
+    assert torch.all(out[4] == 0) and torch.all(torch.isneginf(lse[4]))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_decode_tiny_workload(fmt):
+    w = W.with_format(W.WORKLOADS[0], fmt)
+    cache = build_cache(w, "cuda", gen_device="cpu")
+    qc, qr = W.queries(w)
+    out, lse = Decoder(cache, w.heads, w.seq_len)(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = _oracle_full(w, cache, W.seq_lens(w), qc, qr, "cpu")
+    compare_rows(out, lse, ref_o, ref_l, w.name)
+
+
+FULL = [(1, "C4R4", [0, 19], 6), (2, "C4R4", [3], 8), (3, "C2R4", [0, 40, 63], 6),
+        (4, "C4R4", [1], 8), (4, "C2R4", [2], 6), (4, "BF16", [0], 6)]
+
+
+@pytest.mark.parametrize("cfg,fmt,seqs,nheads", FULL)
+def test_decode_full_size_sampled(cfg, fmt, seqs, nheads):
+    w = W.with_format(W.WORKLOADS[cfg], fmt)
+    lens = W.seq_lens(w)
+    cache = build_cache(w, "cuda", gen_device="cuda")
+    qc, qr = W.queries(w, device="cuda")
+    out, lse = Decoder(cache, w.heads, max(lens))(qc, qr, w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    table = cache.block_table.cpu().numpy()
+    for b in seqs:
+        hs = sample_heads(w.heads, nheads, 100 + b)
+        pool = oracle_pool_for_seq(w, b, lens[b], table[b], cache.num_blocks, "cuda")
+        ro, rl = oracle.decode(W.FORMATS[fmt], pool, table[b:b + 1], np.array([lens[b]]),
+                               qc[b:b + 1, hs].cpu(), qr[b:b + 1, hs].cpu(), w.scale)
+        compare_rows(out[b, hs], lse[b, hs], ro[0], rl[0], f"{w.name} seq {b}")
+
+
+def test_decode_block_permutation_invariance():
+    """Same tokens, different physical block placement: bitwise equal output."""
+    w = _small_workload("C4R4", 128, 12)
+    lens = [700, 64, 130]
+    c1 = build_cache(w, "cuda", lens=lens, permute=True, gen_device="cpu")
+    c2 = build_cache(w, "cuda", lens=lens, permute=False, gen_device="cpu")
+    assert not torch.equal(c1.block_table, c2.block_table)
+    qc, qr = W.queries(w)
+    o1, l1 = Decoder(c1, 128, 700)(qc.cuda(), qr.cuda(), w.scale)
+    o2, l2 = Decoder(c2, 128, 700)(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_decode_deterministic(heads):
+    w = _small_workload("C2R4", heads, 13)
+    lens = [3000, 1, 2000, 640, 64]
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cpu")
+    qc, qr = W.queries(w)
+    dec = Decoder(cache, heads, 3000)
+    o1, l1 = dec(qc.cuda(), qr.cuda(), w.scale)
+    o1, l1 = o1.clone(), l1.clone()
+    o2, l2 = dec(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_decode_bad_block_and_length_are_flagged():
+    w = _small_workload("C4R4", 16, 14)
+    cache = build_cache(w, "cuda", lens=[200, 100], gen_device="cpu")
+    qc, qr = W.queries(w)
+    qc, qr = qc[:2].cuda(), qr[:2].cuda()
+    dec = Decoder(cache, 16, 200)
+    cache.block_table[1, 0] = 10_000  # outside the pool
+    dec(qc, qr, w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() & QMLA_STATUS_BAD_BLOCK
+    cache.status.zero_()
+    cache.block_table.copy_(build_cache(w, "cuda", lens=[200, 100]).block_table)
+    dec2 = Decoder(cache, 16, 150)  # max_seq_len below the first sequence's length
+    out, lse = dec2(qc, qr, w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() & QMLA_STATUS_BAD_LEN
+    assert torch.isfinite(lse).all()
