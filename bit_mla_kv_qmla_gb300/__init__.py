@@ -59,6 +59,8 @@ def qmla_append(fmt, blocks, block_table, positions, latent, rope_k, status,
     """Quantize and pack latent [B][n_new][512] / rope_k [B][n_new][64] (bf16,
     device) into the block pool ``blocks`` (uint8, device)."""
     B, n_new = int(latent.shape[0]), int(latent.shape[1])
+    if block_table.shape[0] < B or positions.numel() < B:
+        raise ValueError("block_table / positions have fewer rows than latent")
     num_blocks = blocks.numel() // qmla_block_bytes(fmt)
     code = _lib.load().qmla_append(
         _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
@@ -75,6 +77,10 @@ def qmla_decode(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r, 
                 out, lse, workspace, status, stream=None) -> None:
     """Absorbed-query MLA decode; writes out [B][H][512] bf16 and lse [B][H] f32."""
     B, H = int(q_c.shape[0]), int(q_c.shape[1])
+    if block_table.shape[0] < B or seq_lens.numel() < B or tuple(q_r.shape[:2]) != (B, H):
+        raise ValueError("block_table / seq_lens / q_r do not cover the query batch")
+    if tuple(out.shape) != (B, H, D_C) or tuple(lse.shape) != (B, H):
+        raise ValueError("out / lse shapes do not match the queries")
     num_blocks = blocks.numel() // qmla_block_bytes(fmt)
     code = _lib.load().qmla_decode(
         _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),

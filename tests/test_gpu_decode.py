@@ -92,8 +92,9 @@ def test_decode_block_permutation_invariance():
     c2 = build_cache(w, "cuda", lens=lens, permute=False, gen_device="cpu")
     assert not torch.equal(c1.block_table, c2.block_table)
     qc, qr = W.queries(w)
-    o1, l1 = Decoder(c1, 128, 700)(qc.cuda(), qr.cuda(), w.scale)
-    o2, l2 = Decoder(c2, 128, 700)(qc.cuda(), qr.cuda(), w.scale)
+    qc, qr = qc[:3].cuda(), qr[:3].cuda()
+    o1, l1 = Decoder(c1, 128, 700)(qc, qr, w.scale)
+    o2, l2 = Decoder(c2, 128, 700)(qc, qr, w.scale)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
