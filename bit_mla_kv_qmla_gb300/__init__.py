@@ -90,6 +90,24 @@ def qmla_decode(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r, 
     _check("qmla_decode", code)
 
 
+def qmla_decode_noalloc(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r,
+                        scale: float, out, lse, status, stream=None) -> None:
+    """qmla_decode without a workspace argument, for callers that cannot
+    allocate: the scratch is the library's fixed per-device array (see
+    include/qmla.h); calls that overlap on the GPU race on it."""
+    B, H = int(q_c.shape[0]), int(q_c.shape[1])
+    if block_table.shape[0] < B or seq_lens.numel() < B or tuple(q_r.shape[:2]) != (B, H):
+        raise ValueError("block_table / seq_lens / q_r do not cover the query batch")
+    if tuple(out.shape) != (B, H, D_C) or tuple(lse.shape) != (B, H):
+        raise ValueError("out / lse shapes do not match the queries")
+    num_blocks = blocks.numel() // qmla_block_bytes(fmt)
+    code = _lib.load().qmla_decode_noalloc(
+        _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
+        _p(seq_lens), int(max_seq_len), B, H, _p(q_c), _p(q_r), float(scale), _p(out), _p(lse),
+        _p(status), _stream(stream))
+    _check("qmla_decode_noalloc", code)
+
+
 def qmla_read_status(status, stream=None) -> int:
     """Synchronize the stream and return QMLA_OK or QMLA_ERR_DEVICE."""
     return int(_lib.load().qmla_read_status(_p(status), _stream(stream)))

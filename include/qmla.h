@@ -185,6 +185,38 @@ int qmla_decode(int format, const void* blocks, int64_t num_blocks,
                 void* workspace, size_t workspace_bytes,
                 int32_t* status_dev, void* stream);
 
+/* Size of the library's own decode scratch used by qmla_decode_noalloc. */
+#define QMLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB per device */
+
+/* qmla_decode_noalloc - qmla_decode for callers that cannot allocate.
+ * The paper has no counterpart to this call; it is a service of this library.
+ * Some callers cannot allocate device memory where they decode: a serving
+ * loop that must not call cudaMalloc once running (it synchronizes the whole
+ * device and can fail under memory pressure), or a plugin whose host only
+ * hands it a stream to enqueue work on.  This call takes the same arguments
+ * as qmla_decode minus the workspace: the split partials and the merge table
+ * go to a fixed QMLA_NOALLOC_SCRATCH_BYTES array in the library's device
+ * memory, which every GPU that loads the library holds until process exit.
+ * Nothing is allocated or freed, by the library or by any other runtime.
+ *   - The first call on a device looks up that array's device address with
+ *     cudaGetSymbolAddress (device current) and keeps it; make that first
+ *     call before capturing the stream into a CUDA graph.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (no part of it needs to start at zero).  Calls whose executions
+ *     overlap on the GPU (on different streams, or concurrently from several
+ *     host threads) race on it: serialize them.
+ *   - When the partials of the usual split do not fit, the context is split
+ *     into fewer pieces; a batch whose merge table plus one partial per
+ *     sequence exceeds the array (roughly batch * heads > 16000 at 512
+ *     channels) returns QMLA_ERR_CAPACITY and enqueues nothing.
+ * Other errors and device status bits as for qmla_decode. */
+int qmla_decode_noalloc(int format, const void* blocks, int64_t num_blocks,
+                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens, int32_t max_seq_len,
+                        int32_t batch, int32_t heads,
+                        const void* q_c, const void* q_r, float softmax_scale,
+                        void* out, float* lse, int32_t* status_dev, void* stream);
+
 /* Synchronize `stream`, read *status_dev and return QMLA_OK if it is 0,
  * QMLA_ERR_DEVICE otherwise (QMLA_ERR_CUDA if the copy failed). */
 int qmla_read_status(const int32_t* status_dev, void* stream);

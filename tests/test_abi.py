@@ -30,7 +30,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["qmla_block_bytes", "qmla_append", "qmla_decode_workspace_bytes",
-                            "qmla_decode", "qmla_read_status", "qmla_error_string"])
+                            "qmla_decode", "qmla_decode_noalloc", "qmla_read_status",
+                            "qmla_error_string"])
 
 
 def test_library_exports_every_declared_symbol(lib):
