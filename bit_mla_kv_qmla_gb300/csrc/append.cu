@@ -4,10 +4,10 @@
 // cache" (flowchart: content quant INT4 or INT2, RoPE quant INT4): each token's
 // 512-channel content latent and 64-channel RoPE key are cut into 64-channel
 // groups, each stored as binary16 (scale, zero) plus packed integer codes.
-// The rounding rules (zero rounded down, scale rounded up, codes rounded half
-// to even) are the ones specified in qmla.h; every step uses an explicitly
-// rounded intrinsic, so the result is bit-exact and independent of
-// compiler contraction.
+// Scale and zero lie on the group's binary16-exact grid and codes are rounded
+// half to even, as specified in qmla.h; every step uses an explicitly rounded
+// intrinsic, so the result is bit-exact and independent of compiler
+// contraction.
 //
 // One CTA per new token, one warp per 64-channel group (8 content + 1 RoPE),
 // each lane holding two consecutive channels.  The whole append is one pass
@@ -29,6 +29,36 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Scale and zero of a group on its binary16-exact grid: the smallest power of
+// two u = 2^E (E in [-24, 5]) with integers Z = floor(mn/u) and
+// M = max(1, ceil((mx - Z*u) / (levels*u))) such that |Z| <= 2047 and
+// |Z + levels*M| <= 2047.  Every dequantized value (Z + c*M)*u is then exactly
+// a binary16 number, so the tensor cores multiply exactly the value the
+// quantizer defines.  Warp uniform; binary64 with explicitly rounded
+// intrinsics (the quotient for M is rounded up, so the bounds hold even when
+// it is inexact).
+__device__ __forceinline__ void group_grid(float mn, float mx, int levels, float& s, float& z) {
+  const double d = __dsub_rd(double(mx), double(mn));
+  int E = (d > 0.0) ? max(-24, ilogb(d) - 12) : -24;
+  for (;; ++E) {
+    const double u = ldexp(1.0, E);
+    double Z = floor(__ddiv_rn(double(mn), u));
+    double M = ceil(__ddiv_ru(__dsub_ru(double(mx), __dmul_rn(Z, u)), __dmul_rn(double(levels), u)));
+    if (M < 1.0) M = 1.0;
+    const bool ok =
+        fabs(Z) <= 2047.0 && fabs(__dadd_rn(Z, __dmul_rn(double(levels), M))) <= 2047.0;
+    if (ok || E >= 5) {
+      if (!ok) {  // outside the |x| < 32768 precondition: clamp into range
+        Z = fmin(2047.0, fmax(-2047.0, Z));
+        M = fmax(1.0, fmin(M, floor(__ddiv_rn(2047.0 - Z, double(levels)))));
+      }
+      z = float(__dmul_rn(Z, u));  // exact
+      s = float(__dmul_rn(M, u));  // exact
+      return;
+    }
+  }
+}
+
 // Quantize the warp's group; lane holds channels 2*lane and 2*lane+1 (x0, x1).
 // Returns the two codes and (scale, zero) as binary16 bits.
 __device__ __forceinline__ void quantize_pair(float x0, float x1, int bits, uint32_t& c0,
@@ -36,23 +66,16 @@ __device__ __forceinline__ void quantize_pair(float x0, float x1, int bits, uint
                                               uint16_t& z_bits) {
   const float mn = warp_min(fminf(x0, x1));
   const float mx = warp_max(fmaxf(x0, x1));
-  const __half z = __float2half_rd(mn);
-  const float zf = __half2float(z);
-  const float r = __fsub_ru(mx, zf);
-  z_bits = __half_as_ushort(z);
-  if (r == 0.0f) {
-    s_bits = 0;
-    c0 = c1 = 0;
-    return;
-  }
-  const float levels = float((1 << bits) - 1);
-  const __half s = __float2half_ru(__fdiv_ru(r, levels));
-  const float sf = __half2float(s);
-  s_bits = __half_as_ushort(s);
+  const int levels = (1 << bits) - 1;
+  float sf, zf;
+  group_grid(mn, mx, levels, sf, zf);
+  s_bits = __half_as_ushort(__float2half_rn(sf));
+  z_bits = __half_as_ushort(__float2half_rn(zf));
+  const float lv = float(levels);
   const float t0 = rintf(__fdiv_rn(__fsub_rn(x0, zf), sf));
   const float t1 = rintf(__fdiv_rn(__fsub_rn(x1, zf), sf));
-  c0 = uint32_t(fminf(fmaxf(t0, 0.0f), levels));
-  c1 = uint32_t(fminf(fmaxf(t1, 0.0f), levels));
+  c0 = uint32_t(fminf(fmaxf(t0, 0.0f), lv));
+  c1 = uint32_t(fminf(fmaxf(t1, 0.0f), lv));
 }
 
 // Pack: the lane's even channel goes to position j of the low half-word, its

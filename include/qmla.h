@@ -23,19 +23,23 @@
  *
  * ---------------------------------------------------------------------------
  * Quantizer (per token, per group of 64 channels, b = 4 or 2 bits,
- * levels = 2^b - 1; all arithmetic IEEE binary32 unless stated):
+ * levels = 2^b - 1):
  *   mn, mx  = min and max of the group (exact)
- *   z       = binary16(mn) rounded toward -inf
- *   r       = mx - float(z), rounded toward +inf
- *   r == 0  -> s = 0 and every code is 0
- *   else    -> s = binary16(r / levels), the division rounded toward +inf and
- *              the conversion rounded toward +inf;
- *              code_i = clamp(rint((x_i - float(z)) / float(s)), 0, levels)
- *              with the subtraction and division rounded to nearest-even and
- *              rint rounding half to even.
- * Directed rounding of z and s makes z <= mn and z + levels*s >= mx, so every
- * element is reproduced within s/2 (plus binary32 rounding) by
- *   x_hat = float(code) * float(s) + float(z).
+ *   grid    = the smallest power of two u = 2^E, -24 <= E <= 5, for which the
+ *             integers Z = floor(mn / u) and
+ *             M = max(1, ceil((mx - Z*u) / (levels*u)))   (quotient rounded up)
+ *             satisfy |Z| <= 2047 and |Z + levels*M| <= 2047; the search starts
+ *             at E = max(-24, ilogb(mx - mn) - 12) (difference rounded down),
+ *             a lower bound, and uses binary64 arithmetic
+ *   z       = Z*u, s = M*u, both stored as binary16 (exactly)
+ *   code_i  = clamp(rint((x_i - z) / s), 0, levels), the subtraction and the
+ *             division in binary32 rounded to nearest-even, rint half to even
+ * Then z <= mn and z + levels*s >= mx, so every element is reproduced within
+ * s/2 (plus binary32 rounding) by x_hat = code*s + z, and every x_hat
+ * (= (Z + code*M)*u, an integer of at most 11 bits times a power of two) is
+ * exactly a binary16 number: the tensor cores multiply exactly the value the
+ * quantizer defines.  For groups containing zero the step s exceeds the ideal
+ * (mx - mn)/levels by at most 16/1023 (INT4) or 4/1023 (INT2) relative.
  *
  * Code packing inside each little-endian 32-bit word (8 INT4 or 16 INT2 codes
  * of consecutive channels c0 .. c0+7 / c0+15): the low 16 bits hold the even

@@ -65,6 +65,12 @@ def lib() -> ctypes.CDLL:
             L.oracle_f32_sub.restype = f32
             L.oracle_f32_div.argtypes = [f32, f32, i32]
             L.oracle_f32_div.restype = f32
+            L.oracle_f64_sub.argtypes = [f64, f64, i32]
+            L.oracle_f64_sub.restype = f64
+            L.oracle_f64_div.argtypes = [f64, f64, i32]
+            L.oracle_f64_div.restype = f64
+            L.oracle_grid_for.argtypes = [f32, f32, i32, P, P, P]
+            L.oracle_grid_for.restype = None
             L.oracle_block_bytes.argtypes = [i32]
             L.oracle_block_bytes.restype = ctypes.c_size_t
             L.oracle_f32_to_f16_array.argtypes = [P, i64, i32, P]
@@ -126,6 +132,23 @@ def f32_sub(a: float, b: float, mode: int) -> float:
 
 def f32_div(a: float, b: float, mode: int) -> float:
     return float(lib().oracle_f32_div(a, b, mode))
+
+
+def f64_sub(a: float, b: float, mode: int) -> float:
+    return float(lib().oracle_f64_sub(a, b, mode))
+
+
+def f64_div(a: float, b: float, mode: int) -> float:
+    return float(lib().oracle_f64_div(a, b, mode))
+
+
+def grid_for(mn: float, mx: float, levels: int):
+    """(E, Z, M) of the binary16-exact grid of a group with range [mn, mx]."""
+    E = ctypes.c_int(0)
+    Z = ctypes.c_double(0)
+    M = ctypes.c_double(0)
+    lib().oracle_grid_for(mn, mx, levels, ctypes.byref(E), ctypes.byref(Z), ctypes.byref(M))
+    return E.value, Z.value, M.value
 
 
 def quantize_group(x: np.ndarray, bits: int):

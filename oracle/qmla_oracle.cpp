@@ -19,9 +19,10 @@
 //    (token, group), 64-token cache blocks, absorbed-query decode
 //    s_t = (q_c . c_t + q_r . k_t) * scale, LSE in natural log.
 //
-// Precision: the quantizer runs in IEEE binary32 with the rounding directions
-// of its specification (directed rounding taken from the CPU's own FPU via
-// fesetround); attention runs in binary64 on the dequantized values.
+// Precision: the quantizer chooses scale and zero on a binary16-exact grid
+// (binary64 arithmetic with directed rounding taken from the CPU's own FPU via
+// fesetround) and computes codes in binary32; attention runs in binary64 on
+// the dequantized values.
 // Build flags must include -frounding-math -ffp-contract=off.
 
 #include <algorithm>
@@ -131,6 +132,24 @@ float f32_div(float a, float b, int mode) {
   return r;
 }
 
+// binary64 subtraction and division with an explicit rounding direction.
+double f64_sub(double a, double b, int mode) {
+  const int old = std::fegetround();
+  std::fesetround(mode == RU ? FE_UPWARD : mode == RD ? FE_DOWNWARD : FE_TONEAREST);
+  volatile double va = a, vb = b;
+  volatile double r = va - vb;
+  std::fesetround(old);
+  return r;
+}
+double f64_div(double a, double b, int mode) {
+  const int old = std::fegetround();
+  std::fesetround(mode == RU ? FE_UPWARD : mode == RD ? FE_DOWNWARD : FE_TONEAREST);
+  volatile double va = a, vb = b;
+  volatile double r = va / vb;
+  std::fesetround(old);
+  return r;
+}
+
 // Round half to even to an integer-valued float.
 float rint_even(float t) {
   const float fl = std::floor(t);
@@ -140,8 +159,41 @@ float rint_even(float t) {
   return (std::fmod(fl, 2.0f) == 0.0f) ? fl : fl + 1.0f;
 }
 
-// Quantize one group of n values to `bits` bits: binary16 scale s and zero z
-// plus integer codes, per the quantizer specification.
+// The binary16-exact grid of a group: the smallest power of two u = 2^E,
+// E in [-24, 5], with integers Z = floor(mn / u) and
+// M = max(1, ceil((mx - Z*u) / (levels*u))) such that |Z| <= 2047 and
+// |Z + levels*M| <= 2047.  Every grid point (Z + c*M)*u, 0 <= c <= levels,
+// is then an integer of at most 11 bits times a power of two: exactly
+// representable in binary16.  E starts at a lower bound (the range needs
+// levels*M*u >= mx - mn with levels*M <= 4094, so u >= (mx - mn) / 2^12); the
+// quotient for M is rounded up, so the bounds hold even when it is inexact.
+// Inputs with |x| >= 32768 (outside the precondition) take E = 5 with Z and M
+// clamped into range.
+void grid_for(float mn, float mx, int levels, int* E_out, double* Z_out, double* M_out) {
+  const double d = f64_sub(mx, mn, RD);
+  int E = (d > 0.0) ? std::max(-24, std::ilogb(d) - 12) : -24;
+  for (;; ++E) {
+    const double u = std::ldexp(1.0, E);
+    double Z = std::floor(double(mn) / u);
+    double M = std::ceil(f64_div(f64_sub(mx, Z * u, RU), levels * u, RU));
+    if (M < 1.0) M = 1.0;
+    const bool ok = std::fabs(Z) <= 2047.0 && std::fabs(Z + levels * M) <= 2047.0;
+    if (ok || E >= 5) {
+      if (!ok) {
+        Z = std::min(2047.0, std::max(-2047.0, Z));
+        M = std::max(1.0, std::min(M, std::floor((2047.0 - Z) / levels)));
+      }
+      *E_out = E;
+      *Z_out = Z;
+      *M_out = M;
+      return;
+    }
+  }
+}
+
+// Quantize one group of n values to `bits` bits: binary16 scale s = M*u and
+// zero z = Z*u on the group's binary16-exact grid, and integer codes
+// c = clamp(rint((x - z) / s), 0, levels) in binary32.
 void quantize_group(const float* x, int n, int bits, uint16_t* s_out,
                     uint16_t* z_out, uint8_t* codes) {
   const int levels = (1 << bits) - 1;
@@ -150,17 +202,12 @@ void quantize_group(const float* x, int n, int bits, uint16_t* s_out,
     if (x[i] < mn) mn = x[i];
     if (x[i] > mx) mx = x[i];
   }
-  const uint16_t z = f32_to_f16(mn, RD);
-  const float zf = f16_to_f32(z);
-  const float r = f32_sub(mx, zf, RU);
-  if (r == 0.0f) {
-    *s_out = 0;
-    *z_out = z;
-    for (int i = 0; i < n; ++i) codes[i] = 0;
-    return;
-  }
-  const uint16_t s = f32_to_f16(f32_div(r, float(levels), RU), RU);
-  const float sf = f16_to_f32(s);
+  int E;
+  double Z, M;
+  grid_for(mn, mx, levels, &E, &Z, &M);
+  const uint16_t z = f32_to_f16(float(Z * std::ldexp(1.0, E)), RN);  // exact
+  const uint16_t s = f32_to_f16(float(M * std::ldexp(1.0, E)), RN);  // exact
+  const float zf = f16_to_f32(z), sf = f16_to_f32(s);
   for (int i = 0; i < n; ++i) {
     const float t = f32_div(f32_sub(x[i], zf, RN), sf, RN);
     float c = rint_even(t);
@@ -341,6 +388,11 @@ uint16_t oracle_f32_to_f16(float x, int mode) { return f32_to_f16(x, mode); }
 float oracle_f16_to_f32(uint16_t h) { return f16_to_f32(h); }
 float oracle_f32_sub(float a, float b, int mode) { return f32_sub(a, b, mode); }
 float oracle_f32_div(float a, float b, int mode) { return f32_div(a, b, mode); }
+double oracle_f64_sub(double a, double b, int mode) { return f64_sub(a, b, mode); }
+double oracle_f64_div(double a, double b, int mode) { return f64_div(a, b, mode); }
+void oracle_grid_for(float mn, float mx, int levels, int* E, double* Z, double* M) {
+  grid_for(mn, mx, levels, E, Z, M);
+}
 
 size_t oracle_block_bytes(int fmt) {
   if (fmt < 0 || fmt > 2) return 0;

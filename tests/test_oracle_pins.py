@@ -137,17 +137,64 @@ def test_quantizer_bounds_and_roundtrip(bits):
     for x in _groups(rng):
         sb, zb, codes = oracle.quantize_group(x, bits)
         s, z = _f16(sb), _f16(zb)
-        assert codes.max() <= levels
+        assert codes.max() <= levels and s > 0
         mn, mx = float(x.min()), float(x.max())
         assert z <= mn
-        if sb == 0:
-            assert mx == z and np.all(codes == 0)
-            continue
         assert z + levels * s >= mx  # exact in float64 (both binary16 values)
         xh = _dequant(codes, s, z).astype(np.float64)
         span = np.maximum(np.abs(x.astype(np.float64)), abs(z) + levels * s)
         slack = 3 * np.spacing(span.astype(np.float32)).astype(np.float64)
         assert np.all(np.abs(x - xh) <= s / 2 + slack)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_quantizer_grid_is_binary16_exact(bits):
+    """Every dequantized value code*s + z is exactly a binary16 number, so a
+    binary16 tensor-core operand carries it without rounding."""
+    rng = np.random.default_rng(50 + bits)
+    levels = (1 << bits) - 1
+    for x in _groups(rng, 400):
+        sb, zb, _ = oracle.quantize_group(x, bits)
+        s, z = _f16(sb), _f16(zb)
+        grid = [Fraction(z) + c * Fraction(s) for c in range(levels + 1)]
+        as16 = np.array([float(g) for g in grid]).astype(np.float16)
+        assert all(Fraction(float(h)) == g for h, g in zip(as16, grid))
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_quantizer_step_is_close_to_range_over_levels(bits):
+    """For groups that contain zero, the grid step is at most (1 + 16/1023)
+    times the ideal (max - min) / levels: the power-of-two unit can be no
+    coarser than max(|min|, max) / 1023.  The unit cannot go below binary16's
+    smallest subnormal 2^-24, which may add up to two such units."""
+    rng = np.random.default_rng(60 + bits)
+    levels = (1 << bits) - 1
+    n = 0
+    for x in _groups(rng, 700):
+        mn, mx = float(x.min()), float(x.max())
+        if not (mn < 0.0 < mx):
+            continue
+        n += 1
+        sb, _, _ = oracle.quantize_group(x, bits)
+        ideal = (mx - mn) / levels
+        bound = max(ideal * (1 + 16 / 1023), ideal + 2 * 2.0**-24)
+        assert _f16(sb) <= bound * (1 + 1e-12)
+    assert n > 100
+
+
+def test_directed_binary64_sub_div():
+    rng = np.random.default_rng(4)
+    a = rng.standard_normal(2000) * np.exp(rng.uniform(-30, 30, 2000))
+    b = rng.standard_normal(2000) * np.exp(rng.uniform(-30, 30, 2000))
+    for x, y in zip(a.tolist(), b.tolist()):
+        for op, fr in ((oracle.f64_sub, Fraction(x) - Fraction(y)),
+                       (oracle.f64_div, Fraction(x) / Fraction(y))):
+            rd, ru = op(x, y, oracle.RD), op(x, y, oracle.RU)
+            assert Fraction(rd) <= fr <= Fraction(ru)
+            if Fraction(rd) == fr:
+                assert rd == ru
+            else:
+                assert np.nextafter(rd, np.inf) == ru
 
 
 @pytest.mark.parametrize("bits", [4, 2])
@@ -180,7 +227,7 @@ def test_quantizer_recovers_exact_grid(bits):
 def test_quantizer_constant_group():
     for v in [0.0, 1.5, -3.25, 1000.0]:
         sb, zb, codes = oracle.quantize_group(np.full(64, v, np.float32), 4)
-        assert sb == 0 and _f16(zb) == v and np.all(codes == 0)
+        assert _f16(sb) > 0 and np.all(_dequant(codes, _f16(sb), _f16(zb)) == np.float32(v))
 
 
 def test_packing_golden():
