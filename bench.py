@@ -260,9 +260,12 @@ def run_ours(args, rank, world, device):
     lens_mid = [L for L in lens_at[0]]
     pk = peaks()
     roof = roofline_for(w.fmt, w.heads, lens_mid, t_dec, pk, recorded_traffic(w.name))
-    roof["kernel"] = "qmla_decode (split-KV decode + combine), CUDA events per call"
     roof["decode_ms"] = round(t_dec * 1e3, 5)
+    tc = w.heads == 128 and w.fmt in ("C4R4", "C2R4")
+    roof["kernel"] = ("decode_tc128 (tcgen05) + plan + combine" if tc else
+                      "decode_simt (CUDA cores) + combine") + ", CUDA events per qmla_decode call"
     res = {"tokens": tokens, "elapsed": elapsed, "t_dec": t_dec, "roofline": roof,
+           "dtype": "f16" if tc else "f32",
            "clocks": clocks, "e2e": e2e, "workload": w, "copies": copies,
            "cache_bytes": cache_bytes, "launches": args.steps * ((1 if n_app else 0) + 2)}
     return res
@@ -448,7 +451,7 @@ def main():
         "metric": METRIC, "value": tok / el, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded, bit_mla_kv_qmla_gb300/workloads.py)",
+        "dtype": res["dtype"], "data": "synthetic (seeded, bit_mla_kv_qmla_gb300/workloads.py)",
         "config": {"workload": w.name, "format": w.fmt, "batch": w.batch, "heads": w.heads,
                    "seq_len": w.seq_len, "append_per_step": max(1, w.n_append),
                    "l2": (f"rotating {res['copies']} cache copies of "

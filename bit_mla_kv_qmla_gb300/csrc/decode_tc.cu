@@ -1,12 +1,572 @@
-// decode_tc.cu - tensor-core (tcgen05) decode kernels.  Placeholder until the
-// kernels land: no head count is served here yet.
-#include "qmla_internal.cuh"
+// decode_tc.cu - tensor-core (tcgen05) decode over the low-bit paged cache,
+// 128 absorbed query heads.
+//
+// The "native low-bit MLA attention kernel" of "QuantMLA: INT4 (and INT2) for
+// both halves of the MLA cache" (flowchart node "Low-bit kernel: dequant
+// inside attention"; "Key findings"): packed blocks are unpacked and
+// dequantized in shared memory and consumed directly by the tensor cores.
+//
+// Work split.  O for 128 heads x 512 channels in binary32 fills the whole
+// 512-column tensor memory of an SM, so one work unit runs on a cluster of
+// two CTAs: CTA r owns content channels 256r..256r+255 and RoPE channels
+// 32r..32r+31, which is exactly one contiguous half of every cache block.
+//   QK : S_r[128 heads x 64 tok] = Qc_r (A, tensor memory) x K_r^T (B, smem)
+//                                + Qr_r (A, smem)          x R_r^T (B, smem)
+//        the two partial scores are exchanged through cluster shared memory
+//        and added (binary32 addition commutes, so both CTAs hold the same
+//        S, the same softmax and the same P);
+//   PV : O_r[128 x 256] += P (A, tensor memory, aliasing S) x C_r (B, the same
+//        dequantized smem tile read MN-major).
+// Tensor memory per CTA: O_r cols 0-255, Qc_r cols 256-383, S/P double
+// buffer cols 384-511.
+//
+// Warp roles (14 warps): 0 bulk-copy producer, 1 MMA issuer (one thread),
+// 2-5 softmax (thread = head), 6-13 dequantization.  Dequantized operands
+// are binary16 (code*scale + zero, exact by construction of the quantizer's
+// grid); queries are converted bf16 -> binary16; accumulation is binary32.
+// The softmax is online in base 2 with lazy rescaling: O and l are rescaled
+// only when a tile's maximum exceeds the running one by more than 8
+// (P <= 256).  Every wait is bounded in time; on timeout the CTA raises an
+// abort flag, all roles unwind, and QMLA_STATUS_TIMEOUT is reported.
+
+#include <cfloat>
+
+#include "plan.cuh"
+#include "tc_ptx.cuh"
 
 namespace qmla {
-int tc_workers(int sms, int heads) { (void)heads; return sms / 2; }
-bool tc_supported(int fmt, int heads) { (void)fmt; (void)heads; return false; }
-cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
-  (void)a; (void)stream;
-  return cudaErrorNotSupported;
+namespace {
+
+using namespace ptx;
+
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
+
+// ---------------------------------------------------------------- planner
+// One warp writes the split plan: merge table, piece descriptors per slot
+// and the slot range of each worker.
+__global__ void __launch_bounds__(32) plan_kernel(DecodeArgs a) {
+  const int lane = threadIdx.x;
+  int64_t N = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    N += warp_sum((b < a.batch) ? seq_blocks(a, b, true) : 0);
+  }
+  const int64_t P = plan_workers(N, a.workers);  // every planned worker owns >= 1 block
+  for (int64_t w = P + lane; w < a.workers; w += 32) a.ws.wrange[w] = make_int2(0, -1);
+  int64_t carry_blocks = 0;
+  int carry_slots = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    const int nb = (b < a.batch) ? seq_blocks(a, b, false) : 0;
+    const int incl = warp_incl_scan(nb);
+    const int64_t S = carry_blocks + (incl - nb);
+    int np = 0;
+    int64_t pf = 0;
+    if (nb > 0) {
+      pf = plan_owner(S, N, P);
+      np = int(plan_owner(S + nb - 1, N, P) - pf + 1);
+    }
+    const int np_incl = warp_incl_scan(np);
+    const int base = carry_slots + (np_incl - np);
+    if (b < a.batch) a.ws.seq_table[b] = make_int2(base, np);
+    for (int i = 0; i < np; ++i) {
+      const int64_t w = pf + i;
+      const int64_t w0 = plan_start(w, N, P), w1 = plan_start(w + 1, N, P);
+      const int j0 = int(max(w0 - S, int64_t(0))), j1 = int(min(w1 - S, int64_t(nb)));
+      a.ws.pieces[base + i] = make_int4(b, j0, j1, 0);
+      if (w0 >= S) a.ws.wrange[w].x = base + i;       // the worker's first piece
+      if (w1 <= S + nb) a.ws.wrange[w].y = base + i;  // the worker's last piece
+    }
+    carry_blocks += __shfl_sync(0xffffffffu, incl, 31);
+    carry_slots += __shfl_sync(0xffffffffu, np_incl, 31);
+  }
 }
+
+// ---------------------------------------------------------------- layout
+constexpr int kThreads = 448;
+constexpr int kMmaWarp = 1;
+constexpr int kSoftmaxWarp0 = 2;
+constexpr int kDequantWarp0 = 6;
+constexpr int kDequantThreads = 256;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
+
+constexpr uint32_t kSmQr = 0;                        // [128 heads][128 B] SW128, 16 KB
+constexpr uint32_t kSmK = 16384;                     // 2 x K tile
+constexpr uint32_t kChunk = 8192;                    // [64 tok][64 ch] fp16 SW128
+constexpr uint32_t kKTile = 5 * kChunk;              // 4 content chunks + RoPE chunk
+constexpr uint32_t kSmStage = kSmK + 2 * kKTile;     // 2 x staging
+constexpr uint32_t kStage = 10240 + 256;             // largest half + RoPE scale/zero
+constexpr uint32_t kSmX = kSmStage + 2 * kStage;     // 2 x score exchange
+constexpr uint32_t kX = 128 * 64 * 4;
+constexpr uint32_t kSmBar = kSmX + 2 * kX;
+constexpr uint32_t kNumBars = 20;
+constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
+constexpr uint32_t kSmAbort = kSmTslot + 4;
+constexpr uint32_t kSmBytes = kSmAbort + 60;
+constexpr uint32_t kSmDyn = kSmBytes + 1024;         // slack for 1 KB alignment
+
+// barrier indices
+enum : uint32_t {
+  B_STAGE_FULL = 0, B_STAGE_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 6, B_S_FULL = 8,
+  B_P_FULL = 10, B_PV_DONE = 12, B_X_FULL = 14, B_X_EMPTY = 16, B_Q_FULL = 18, B_DRAIN = 19
+};
+
+__device__ __forceinline__ bool wait_noabort(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitNs) return false;
+  return true;
+}
+// All lanes of the warp agree on the outcome of a wait, so that the warp stays
+// converged for the warp-synchronous tensor-memory instructions that follow.
+__device__ __forceinline__ bool warp_ok(bool v) { return __all_sync(0xffffffffu, v); }
+
+// Four pairs of binary16 values (channels 2k, 2k+1) from 8 INT4 codes packed
+// even-low / odd-high: x = code * s + z (exact on the quantizer's grid).
+__device__ __forceinline__ void dq_int4(uint32_t w, __half2 s2, __half2 z2, uint32_t* out) {
+  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t v = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), magic);
+    h = __hfma2(h, s2, z2);
+    out[k] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+// Eight pairs from 16 INT2 codes.
+__device__ __forceinline__ void dq_int2(uint32_t w, __half2 s2, __half2 z2, uint32_t* out) {
+  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t v = ((w >> (2 * k)) & 0x00030003u) | 0x64006400u;
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), magic);
+    h = __hfma2(h, s2, z2);
+    out[k] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+__device__ __forceinline__ void split_sz(uint32_t sz, __half2& s2, __half2& z2) {
+  const __half s = __ushort_as_half(uint16_t(sz & 0xffffu));
+  const __half z = __ushort_as_half(uint16_t(sz >> 16));
+  s2 = __halves2half2(s, s);
+  z2 = __halves2half2(z, z);
+}
+// 16 channels (8 words) into row `row` of an SW128 [rows][64 fp16] region,
+// logical 16-byte granules 2*seg and 2*seg+1.
+__device__ __forceinline__ void st_row16(unsigned char* region, int row, int seg,
+                                         const uint32_t* v) {
+  unsigned char* r = region + (row >> 3) * 1024 + (row & 7) * 128;
+  *reinterpret_cast<uint4*>(r + (((2 * seg) ^ (row & 7)) << 4)) =
+      make_uint4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<uint4*>(r + (((2 * seg + 1) ^ (row & 7)) << 4)) =
+      make_uint4(v[4], v[5], v[6], v[7]);
+}
+
+// Valid tokens of block j of sequence b (0 for a block id outside the pool).
+__device__ __forceinline__ int tile_tokens(const DecodeArgs& a, int b, int j) {
+  const int32_t blk = a.block_table[int64_t(b) * a.max_blocks_per_seq + j];
+  if (blk < 0 || blk >= a.num_blocks) return 0;
+  return min(kT, seq_len_clamped(a, b) - j * kT);
+}
+
+// ---------------------------------------------------------------- kernel
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc128_kernel(DecodeArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb0 = smem_u32(sm);
+  auto BAR = [&](uint32_t i) { return sb0 + kSmBar + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  const int pair = blockIdx.x >> 1;
+  const Geom G = geom(a.fmt);
+
+  if (threadIdx.x == 0) {
+    for (uint32_t i = 0; i < 2; ++i) {
+      mbar_init(BAR(B_STAGE_FULL + i), 1);
+      mbar_init(BAR(B_STAGE_EMPTY + i), kDequantThreads / 32);
+      mbar_init(BAR(B_K_FULL + i), kDequantThreads / 32);
+      mbar_init(BAR(B_K_EMPTY + i), 1);
+      mbar_init(BAR(B_S_FULL + i), 1);
+      mbar_init(BAR(B_P_FULL + i), 128);
+      mbar_init(BAR(B_PV_DONE + i), 1);
+      mbar_init(BAR(B_X_FULL + i), 128);
+      mbar_init(BAR(B_X_EMPTY + i), 128);
+    }
+    mbar_init(BAR(B_Q_FULL), 128);
+    mbar_init(BAR(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(sb0 + kSmTslot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialized before any remote arrive
+  tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kSmTslot);
+  const int2 wr = a.ws.wrange[pair];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t t = 0;
+      bool ok = true;
+      for (int s = wr.x; ok && s <= wr.y; ++s) {
+        const int4 pc = a.ws.pieces[s];
+        for (int j = pc.y; j < pc.z; ++j, ++t) {
+          const uint32_t st = t & 1u, par = (t >> 1) & 1u;
+          if (!mbar_wait(BAR(B_STAGE_EMPTY + st), par ^ 1u, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          const int32_t blk = a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + j];
+          const uint32_t dst = sb0 + kSmStage + st * kStage;
+          if (blk >= 0 && blk < a.num_blocks) {
+            const unsigned char* src = a.blocks + int64_t(blk) * G.block;
+            mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), uint32_t(G.half) + 256u);
+            bulk_g2s(dst, src + rank * G.half, uint32_t(G.half), BAR(B_STAGE_FULL + st));
+            bulk_g2s(dst + G.half, src + G.rope_sz_off, 256u, BAR(B_STAGE_FULL + st));
+          } else {
+            set_status(a.status, QMLA_STATUS_BAD_BLOCK);
+            mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), 0u);
+          }
+        }
+      }
+      // copies still in flight must land before the CTA can exit
+      for (uint32_t u = (t >= 2 ? t - 2 : 0); u < t; ++u)
+        wait_noabort(BAR(B_STAGE_FULL + (u & 1u)), (u >> 1) & 1u);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_f16(128, 64, false, false);
+      const uint32_t idesc_pv = idesc_f16(128, 256, false, true);
+      uint32_t t = 0, piece = 0;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t tt, bool first) {
+        const uint32_t sb = tt & 1u;
+        const uint32_t kt = sb0 + kSmK + sb * kKTile;
+#pragma unroll
+        for (uint32_t kk = 0; kk < 4; ++kk) {
+          mma_ts(tbase + kColO, tbase + kColS + 64 * sb + 8 * kk,
+                 smem_desc(kt + kk * 2048, kChunk, 1024, kSwizzle128B), idesc_pv,
+                 (first && kk == 0) ? 0u : 1u);
+        }
+        mma_commit(BAR(B_PV_DONE + sb));
+        mma_commit(BAR(B_K_EMPTY + sb));
+      };
+      for (int s = wr.x; ok && s <= wr.y; ++s) {
+        const int4 pc = a.ws.pieces[s];
+        if (pc.z <= pc.y) continue;
+        if (!mbar_wait(BAR(B_Q_FULL), piece & 1u, abort_flag, kWaitNs)) break;
+        ++piece;
+        tc_fence_after();
+        for (int j = pc.y; j < pc.z; ++j, ++t) {
+          const uint32_t sb = t & 1u, par = (t >> 1) & 1u;
+          if (!mbar_wait(BAR(B_K_FULL + sb), par, abort_flag, kWaitNs) ||
+              (t >= 2 && !mbar_wait(BAR(B_PV_DONE + sb), par ^ 1u, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kt = sb0 + kSmK + sb * kKTile;
+          const uint32_t d = tbase + kColS + 64 * sb;
+#pragma unroll
+          for (uint32_t kc = 0; kc < 16; ++kc)
+            mma_ts(d, tbase + kColQ + 8 * kc,
+                   smem_desc(kt + (kc >> 2) * kChunk + (kc & 3) * 32, 16, 1024, kSwizzle128B),
+                   idesc_qk, kc > 0 ? 1u : 0u);
+#pragma unroll
+          for (uint32_t kr = 0; kr < 2; ++kr)
+            mma_ss(d, smem_desc(sb0 + kSmQr + kr * 32, 16, 1024, kSwizzle128B),
+                   smem_desc(kt + 4 * kChunk + kr * 32, 16, 1024, kSwizzle128B), idesc_qk, 1u);
+          mma_commit(BAR(B_S_FULL + sb));
+          if (j > pc.y) {
+            const uint32_t tp = t - 1;
+            if (!mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(tp, j - 1 == pc.y);
+          }
+        }
+        if (!ok) break;
+        const uint32_t tp = t - 1;
+        if (!mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag, kWaitNs)) break;
+        tc_fence_after();
+        issue_pv(tp, pc.z - 1 == pc.y);
+      }
+      // no MMA may be in flight when tensor memory is released
+      mma_commit(BAR(B_DRAIN));
+      wait_noabort(BAR(B_DRAIN), 0);
+    }
+  } else if (warp >= kSoftmaxWarp0 && warp < kDequantWarp0) {
+    // ------------------------------------------------------------ softmax
+    const uint32_t quad = uint32_t(warp & 3);
+    const int h = int(quad * 32) + lane;
+    const uint32_t lane_base = (quad * 32u) << 16;
+    const float c2 = a.scale * 1.4426950408889634f;  // scores to log2 units
+    uint32_t t = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      const int b = pc.x;
+      if (pc.z <= pc.y) {  // no block: an empty partial (the planner produces none)
+        for (int c = 0; c < 256; ++c) a.ws.part_o[(int64_t(s) * 128 + h) * kDc + 256 * rank + c] = 0.f;
+        if (rank == 0) a.ws.part_lse[int64_t(s) * 128 + h] = -INFINITY;
+        continue;
+      }
+      // queries of this piece: Qc half -> tensor memory, Qr half -> smem
+      {
+        const __nv_bfloat16* qrow = a.q_c + (int64_t(b) * 128 + h) * kDc + 256 * rank;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 64) {
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + c0 + 8 * i);
+            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              w[4 * i + k] = pack_half2(__uint_as_float(in[k] << 16),
+                                        __uint_as_float(in[k] & 0xffff0000u));
+          }
+          tmem_st32(tbase + lane_base + kColQ + c0 / 2, w);
+        }
+        const __nv_bfloat16* rrow = a.q_r + (int64_t(b) * 128 + h) * kDr + 32 * rank;
+        unsigned char* qr = sm + kSmQr + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rrow + 8 * g);
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xffff0000u));
+          *reinterpret_cast<uint4*>(qr + ((g ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(B_Q_FULL));
+      }
+      float m_run = -INFINITY, l_run = 0.0f;
+      for (int j = pc.y; j < pc.z; ++j, ++t) {
+        const uint32_t sb = t & 1u, par = (t >> 1) & 1u;
+        if (!warp_ok(mbar_wait(BAR(B_S_FULL + sb), par, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tbase + lane_base + kColS + 64 * sb, r0);
+          tmem_ld32(tbase + lane_base + kColS + 64 * sb + 32, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            sv[i] = __uint_as_float(r0[i]);
+            sv[32 + i] = __uint_as_float(r1[i]);
+          }
+        }
+        // exchange partial scores with the peer CTA
+        if (!warp_ok(mbar_wait<true>(BAR(B_X_EMPTY + sb), par ^ 1u, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        const uint32_t xrow = kSmX + sb * kX + uint32_t(h) * 256u;
+        const uint32_t prow = mapa(sb0 + xrow, peer);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          st_cluster_v4(prow + ((uint32_t(q) ^ uint32_t(h & 15)) << 4), sv[4 * q], sv[4 * q + 1],
+                        sv[4 * q + 2], sv[4 * q + 3]);
+        mbar_arrive_remote(mapa(BAR(B_X_FULL + sb), peer));
+        if (!warp_ok(mbar_wait<true>(BAR(B_X_FULL + sb), par, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(sm + xrow + ((q ^ (h & 15)) << 4));
+          sv[4 * q] += v.x;
+          sv[4 * q + 1] += v.y;
+          sv[4 * q + 2] += v.z;
+          sv[4 * q + 3] += v.w;
+        }
+        mbar_arrive_remote(mapa(BAR(B_X_EMPTY + sb), peer));
+
+        const int nvalid = tile_tokens(a, b, j);
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          sv[i] = (i < nvalid) ? sv[i] * c2 : -INFINITY;
+          mt = fmaxf(mt, sv[i]);
+        }
+        const bool need = mt > m_run + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mt : m_run;
+          const float alpha = need ? exp2f(m_run - m_new) : 1.0f;
+          if (j > pc.y) {
+            const uint32_t tp = t - 1;
+            if (!warp_ok(mbar_wait(BAR(B_PV_DONE + (tp & 1u)), (tp >> 1) & 1u, abort_flag,
+                                   kWaitNs))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tbase + lane_base + kColO + c0, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tbase + lane_base + kColO + c0, o);
+            }
+            tmem_wait_st();
+          }
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        uint32_t pk[32];
+        float ls = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = (mt == -INFINITY) ? 0.0f : exp2f(sv[2 * i] - m_run);
+          const float p1 = (mt == -INFINITY) ? 0.0f : exp2f(sv[2 * i + 1] - m_run);
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          ls += __low2float(hp) + __high2float(hp);
+          pk[i] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        l_run += ls;
+        tmem_st32(tbase + lane_base + kColS + 64 * sb, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(B_P_FULL + sb));
+      }
+      if (!ok) break;
+      // epilogue: normalized partial O (this CTA's 256 channels) and LSE
+      const uint32_t tl = t - 1;
+      if (!warp_ok(mbar_wait(BAR(B_PV_DONE + (tl & 1u)), (tl >> 1) & 1u, abort_flag, kWaitNs)))
+        break;
+      tc_fence_after();
+      const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      float* orow = a.ws.part_o + (int64_t(s) * 128 + h) * kDc + 256 * rank;
+#pragma unroll 1
+      for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tbase + lane_base + kColO + c0, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(orow + c0 + i) =
+              make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                          __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+      }
+      if (rank == 0)
+        a.ws.part_lse[int64_t(s) * 128 + h] =
+            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      tc_fence_before();
+    }
+  } else if (warp >= kDequantWarp0) {
+    // ------------------------------------------------------------ dequant
+    const int dt = int(threadIdx.x) - kDequantWarp0 * 32;
+    uint32_t t = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      for (int j = pc.y; j < pc.z; ++j, ++t) {
+        const uint32_t st = t & 1u, kb = t & 1u, par = (t >> 1) & 1u;
+        bool got = mbar_wait(BAR(B_STAGE_FULL + st), par, abort_flag, kWaitNs);
+        got = got && mbar_wait(BAR(B_K_EMPTY + kb), par ^ 1u, abort_flag, kWaitNs);
+        if (!warp_ok(got)) {
+          ok = false;
+          break;
+        }
+        const int nvalid = tile_tokens(a, pc.x, j);
+        const unsigned char* stg = sm + kSmStage + st * kStage;
+        unsigned char* kt = sm + kSmK + kb * kKTile;
+        // content: 4 groups x 64 tokens x 4 segments of 16 channels
+#pragma unroll 1
+        for (int it = dt; it < 1024; it += kDequantThreads) {
+          const int g = it >> 8, tt = (it >> 2) & 63, seg = it & 3;
+          uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          if (tt < nvalid) {
+            __half2 s2, z2;
+            split_sz(*reinterpret_cast<const uint32_t*>(stg + G.sz_off + (g * 64 + tt) * 4), s2,
+                     z2);
+            if (G.cbits == 4) {
+              const uint2 w = *reinterpret_cast<const uint2*>(stg + g * 2048 + tt * 32 + seg * 8);
+              dq_int4(w.x, s2, z2, v);
+              dq_int4(w.y, s2, z2, v + 4);
+            } else {
+              dq_int2(*reinterpret_cast<const uint32_t*>(stg + g * 1024 + tt * 16 + seg * 4), s2,
+                      z2, v);
+            }
+          }
+          st_row16(kt + g * kChunk, tt, seg, v);
+        }
+        // RoPE: 64 tokens x 2 segments of 16 channels (INT4)
+        if (dt < 128) {
+          const int tt = dt >> 1, seg = dt & 1;
+          uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          if (tt < nvalid) {
+            __half2 s2, z2;
+            split_sz(*reinterpret_cast<const uint32_t*>(stg + G.half + tt * 4), s2, z2);
+            const uint2 w = *reinterpret_cast<const uint2*>(stg + G.rope_off + tt * 16 + seg * 8);
+            dq_int4(w.x, s2, z2, v);
+            dq_int4(w.y, s2, z2, v + 4);
+          }
+          st_row16(kt + 4 * kChunk, tt, seg, v);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(BAR(B_K_FULL + kb));
+          mbar_arrive(BAR(B_STAGE_EMPTY + st));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) set_status(a.status, QMLA_STATUS_TIMEOUT);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+  cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
+}
+
+}  // namespace
+
+int tc_workers(int sms, int heads) {
+  (void)heads;
+  return sms / 2 > 0 ? sms / 2 : 1;
+}
+
+bool tc_supported(int fmt, int heads) {
+  return heads == 128 && (fmt == QMLA_C4R4 || fmt == QMLA_C2R4);
+}
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
+  plan_kernel<<<1, 32, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kSmDyn));
+  if (e != cudaSuccess) return e;
+  decode_tc128_kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace qmla

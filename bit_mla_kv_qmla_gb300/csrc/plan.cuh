@@ -2,9 +2,9 @@
 //
 // The context of every sequence is attended in pieces (split-KV); the pieces
 // are merged afterwards by log-sum-exp.  All sequences' 64-token blocks are
-// concatenated in sequence order and cut into P near-equal contiguous ranges,
-// one per worker, so every worker gets the same number of blocks whatever the
-// length mix.  One warp scans seq_lens (32 sequences per step) with warp
+// concatenated in sequence order and cut into min(P, N) near-equal contiguous
+// ranges, one per worker, so every worker gets the same number of blocks
+// whatever the length mix, and no planned worker is empty.  One warp scans seq_lens (32 sequences per step) with warp
 // prefix sums; no host-side copy of the lengths is needed.
 #pragma once
 
@@ -76,8 +76,9 @@ __device__ __forceinline__ int64_t plan_total(const DecodeArgs& a) {
 __device__ __forceinline__ bool plan_next(const DecodeArgs& a, PlanState& st, int64_t w,
                                           bool publish) {
   const int lane = threadIdx.x & 31;
-  const int64_t N = st.total_blocks, P = a.workers;
-  const int64_t g0 = plan_start(w, N, P), g1 = plan_start(w + 1, N, P);
+  const int64_t N = st.total_blocks, P = plan_workers(N, a.workers);
+  const int64_t g0 = (w < P) ? plan_start(w, N, P) : N;
+  const int64_t g1 = (w < P) ? plan_start(w + 1, N, P) : N;
   if (lane == 0) st.n = 0;
   __syncwarp();
   if (st.next_seq >= a.batch || (!publish && st.carry_blocks >= g1)) return false;

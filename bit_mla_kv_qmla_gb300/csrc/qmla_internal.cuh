@@ -45,30 +45,41 @@ __device__ __forceinline__ void set_status(int32_t* status, int bits) {
 __host__ __device__ __forceinline__ int blocks_of(int L) { return (L + kT - 1) / kT; }
 
 // Split plan.  The blocks of all sequences, concatenated in sequence order,
-// are cut into P contiguous ranges of near-equal size, one per worker (CTA or
-// CTA pair).  Worker w owns global blocks [start(w), start(w+1)) with
-// start(w) = floor(w*N/P).  A worker range that touches k sequences produces
-// k partial results ("pieces").  Pieces of sequence b get consecutive slots
-// base_b .. base_b + n_b - 1 of the partial buffers.
-__host__ __device__ __forceinline__ int64_t plan_start(int64_t w, int64_t N, int64_t P) {
-  return (w * N) / P;
+// are cut into Pe = min(P, N) contiguous ranges of near-equal size, one per
+// worker (CTA or CTA pair), so every planned worker owns at least one block;
+// workers >= Pe get nothing.  Worker w < Pe owns global blocks
+// [start(w), start(w+1)) with start(w) = floor(w*N/Pe).  A worker range that
+// touches k sequences produces k partial results ("pieces"); the pieces of
+// sequence b get consecutive slots base_b .. base_b + n_b - 1.
+__host__ __device__ __forceinline__ int64_t plan_workers(int64_t N, int64_t P) {
+  return N < P ? N : P;
 }
-// Worker owning global block g (0 <= g < N).
-__host__ __device__ __forceinline__ int64_t plan_owner(int64_t g, int64_t N, int64_t P) {
-  return ((g + 1) * P - 1) / N;
+__host__ __device__ __forceinline__ int64_t plan_start(int64_t w, int64_t N, int64_t Pe) {
+  return Pe > 0 ? (w * N) / Pe : 0;
+}
+// Worker owning global block g (0 <= g < N, Pe >= 1).
+__host__ __device__ __forceinline__ int64_t plan_owner(int64_t g, int64_t N, int64_t Pe) {
+  return ((g + 1) * Pe - 1) / N;
 }
 
-// Workspace layout for the decode: [seq table B x int2][part LSE slots x H]
-// [part O slots x H x 512] (each region 256-byte aligned).
+// Workspace layout for the decode (each region 256-byte aligned):
+//   seq table  [B] int2   (first slot, number of pieces) per sequence
+//   part LSE   [slots][H] float
+//   part O     [slots][H][512] float
+//   pieces     [slots] int4 (sequence, first block, end block, 0) per slot
+//   worker     [slots] int2 (first slot, last slot) per worker (P <= slots)
 struct Workspace {
-  int2* seq_table;  // (first slot, number of pieces) per sequence
+  int2* seq_table;
   float* part_lse;
   float* part_o;
+  int4* pieces;
+  int2* wrange;
 };
 __host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 __host__ __device__ __forceinline__ size_t workspace_bytes(int batch, int heads, int slots) {
   return align256(size_t(batch) * sizeof(int2)) + align256(size_t(slots) * heads * sizeof(float)) +
-         align256(size_t(slots) * heads * kDc * sizeof(float));
+         align256(size_t(slots) * heads * kDc * sizeof(float)) +
+         align256(size_t(slots) * sizeof(int4)) + align256(size_t(slots) * sizeof(int2));
 }
 __host__ __device__ __forceinline__ Workspace carve(void* ws, int batch, int heads, int slots) {
   char* p = static_cast<char*>(ws);
@@ -78,6 +89,10 @@ __host__ __device__ __forceinline__ Workspace carve(void* ws, int batch, int hea
   w.part_lse = reinterpret_cast<float*>(p);
   p += align256(size_t(slots) * heads * sizeof(float));
   w.part_o = reinterpret_cast<float*>(p);
+  p += align256(size_t(slots) * heads * kDc * sizeof(float));
+  w.pieces = reinterpret_cast<int4*>(p);
+  p += align256(size_t(slots) * sizeof(int4));
+  w.wrange = reinterpret_cast<int2*>(p);
   return w;
 }
 
