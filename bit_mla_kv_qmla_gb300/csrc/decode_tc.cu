@@ -13,8 +13,9 @@
 //   QK : S_r[128 heads x 64 tok] = Qc_r (A, tensor memory) x K_r^T (B, smem)
 //                                + Qr_r (A, smem)          x R_r^T (B, smem)
 //        the two partial scores are exchanged through cluster shared memory
-//        and added (binary32 addition commutes, so both CTAs hold the same
-//        S, the same softmax and the same P);
+//        with asynchronous remote stores that complete on the receiver's
+//        mbarrier, and added (binary32 addition commutes, so both CTAs hold
+//        the same S, the same softmax and the same P);
 //   PV : O_r[128 x 256] += P (A, tensor memory, aliasing S) x C_r (B, the same
 //        dequantized smem tile read MN-major).
 // Tensor memory per CTA: O_r cols 0-255, Qc_r cols 256-383, S/P double
@@ -96,12 +97,13 @@ constexpr uint32_t kSmQr = 0;                        // [128 heads][128 B] SW128
 constexpr uint32_t kSmK = 16384;                     // 2 x K tile
 constexpr uint32_t kChunk = 8192;                    // [64 tok][64 ch] fp16 SW128
 constexpr uint32_t kKTile = 5 * kChunk;              // 4 content chunks + RoPE chunk
-constexpr uint32_t kSmStage = kSmK + 2 * kKTile;     // 2 x staging
+constexpr uint32_t kStages = 4;                      // bulk-copy ring depth
+constexpr uint32_t kSmStage = kSmK + 2 * kKTile;     // kStages x staging
 constexpr uint32_t kStage = 10240 + 256;             // largest half + RoPE scale/zero
-constexpr uint32_t kSmX = kSmStage + 2 * kStage;     // 2 x score exchange
+constexpr uint32_t kSmX = kSmStage + kStages * kStage;  // 2 x score exchange
 constexpr uint32_t kX = 128 * 64 * 4;
 constexpr uint32_t kSmBar = kSmX + 2 * kX;
-constexpr uint32_t kNumBars = 20;
+constexpr uint32_t kNumBars = 24;
 constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
 constexpr uint32_t kSmBytes = kSmAbort + 60;
@@ -109,8 +111,8 @@ constexpr uint32_t kSmDyn = kSmBytes + 1024;         // slack for 1 KB alignment
 
 // barrier indices
 enum : uint32_t {
-  B_STAGE_FULL = 0, B_STAGE_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 6, B_S_FULL = 8,
-  B_P_FULL = 10, B_PV_DONE = 12, B_X_FULL = 14, B_X_EMPTY = 16, B_Q_FULL = 18, B_DRAIN = 19
+  B_STAGE_FULL = 0, B_STAGE_EMPTY = 4, B_K_FULL = 8, B_K_EMPTY = 10, B_S_FULL = 12,
+  B_P_FULL = 14, B_PV_DONE = 16, B_X_FULL = 18, B_X_EMPTY = 20, B_Q_FULL = 22, B_DRAIN = 23
 };
 
 __device__ __forceinline__ bool wait_noabort(uint32_t bar, uint32_t parity) {
@@ -163,11 +165,18 @@ __device__ __forceinline__ void st_row16(unsigned char* region, int row, int seg
       make_uint4(v[4], v[5], v[6], v[7]);
 }
 
-// Valid tokens of block j of sequence b (0 for a block id outside the pool).
-__device__ __forceinline__ int tile_tokens(const DecodeArgs& a, int b, int j) {
-  const int32_t blk = a.block_table[int64_t(b) * a.max_blocks_per_seq + j];
-  if (blk < 0 || blk >= a.num_blocks) return 0;
-  return min(kT, seq_len_clamped(a, b) - j * kT);
+// Validity of blocks j0 .. j0+31 of sequence b as a bit mask (bit k: block
+// j0+k exists in the piece and its id lies inside the pool).  One coalesced
+// load per warp for 32 tiles keeps global-memory latency out of the per-tile
+// path.  Called by a full warp.
+__device__ __forceinline__ uint32_t valid_mask(const DecodeArgs& a, int b, int j0, int j1) {
+  const int j = j0 + int(threadIdx.x & 31);
+  bool ok = false;
+  if (j < j1) {
+    const int32_t blk = a.block_table[int64_t(b) * a.max_blocks_per_seq + j];
+    ok = blk >= 0 && blk < a.num_blocks;
+  }
+  return __ballot_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -185,19 +194,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const Geom G = geom(a.fmt);
 
   if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < 2; ++i) {
+    for (uint32_t i = 0; i < kStages; ++i) {
       mbar_init(BAR(B_STAGE_FULL + i), 1);
       mbar_init(BAR(B_STAGE_EMPTY + i), kDequantThreads / 32);
+    }
+    for (uint32_t i = 0; i < 2; ++i) {
       mbar_init(BAR(B_K_FULL + i), kDequantThreads / 32);
       mbar_init(BAR(B_K_EMPTY + i), 1);
       mbar_init(BAR(B_S_FULL + i), 1);
       mbar_init(BAR(B_P_FULL + i), 128);
       mbar_init(BAR(B_PV_DONE + i), 1);
-      mbar_init(BAR(B_X_FULL + i), 128);
+      mbar_init(BAR(B_X_FULL + i), 1);
       mbar_init(BAR(B_X_EMPTY + i), 128);
     }
     mbar_init(BAR(B_Q_FULL), 128);
     mbar_init(BAR(B_DRAIN), 1);
+    // the first two score exchanges are expected before the peer can send them
+    mbar_arrive_expect_tx(BAR(B_X_FULL + 0), kX);
+    mbar_arrive_expect_tx(BAR(B_X_FULL + 1), kX);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -214,34 +228,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t t = 0;
-      bool ok = true;
-      for (int s = wr.x; ok && s <= wr.y; ++s) {
-        const int4 pc = a.ws.pieces[s];
-        for (int j = pc.y; j < pc.z; ++j, ++t) {
-          const uint32_t st = t & 1u, par = (t >> 1) & 1u;
-          if (!mbar_wait(BAR(B_STAGE_EMPTY + st), par ^ 1u, abort_flag, kWaitNs)) {
+    uint32_t t = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      for (int jb = pc.y; ok && jb < pc.z; jb += 32) {
+        const int n = min(32, pc.z - jb);
+        const int32_t my_blk =
+            (lane < n) ? a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + jb + lane] : -1;
+        for (int k = 0; k < n; ++k, ++t) {
+          const int32_t blk = __shfl_sync(0xffffffffu, my_blk, k);
+          bool got = true;
+          if (lane == 0) {
+            const uint32_t st = t % kStages, par = (t / kStages) & 1u;
+            got = mbar_wait(BAR(B_STAGE_EMPTY + st), par ^ 1u, abort_flag, kWaitNs);
+            if (got) {
+              const uint32_t dst = sb0 + kSmStage + st * kStage;
+              if (blk >= 0 && blk < a.num_blocks) {
+                const unsigned char* src = a.blocks + int64_t(blk) * G.block;
+                mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), uint32_t(G.half) + 256u);
+                bulk_g2s(dst, src + rank * G.half, uint32_t(G.half), BAR(B_STAGE_FULL + st));
+                bulk_g2s(dst + G.half, src + G.rope_sz_off, 256u, BAR(B_STAGE_FULL + st));
+              } else {
+                set_status(a.status, QMLA_STATUS_BAD_BLOCK);
+                mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), 0u);
+              }
+            }
+          }
+          if (!warp_ok(got)) {
             ok = false;
             break;
           }
-          const int32_t blk = a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + j];
-          const uint32_t dst = sb0 + kSmStage + st * kStage;
-          if (blk >= 0 && blk < a.num_blocks) {
-            const unsigned char* src = a.blocks + int64_t(blk) * G.block;
-            mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), uint32_t(G.half) + 256u);
-            bulk_g2s(dst, src + rank * G.half, uint32_t(G.half), BAR(B_STAGE_FULL + st));
-            bulk_g2s(dst + G.half, src + G.rope_sz_off, 256u, BAR(B_STAGE_FULL + st));
-          } else {
-            set_status(a.status, QMLA_STATUS_BAD_BLOCK);
-            mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), 0u);
-          }
         }
       }
-      // copies still in flight must land before the CTA can exit
-      for (uint32_t u = (t >= 2 ? t - 2 : 0); u < t; ++u)
-        wait_noabort(BAR(B_STAGE_FULL + (u & 1u)), (u >> 1) & 1u);
     }
+    // copies still in flight must land before the CTA can exit
+    if (lane == 0)
+      for (uint32_t u = (t >= kStages ? t - kStages : 0); u < t; ++u)
+        wait_noabort(BAR(B_STAGE_FULL + u % kStages), (u / kStages) & 1u);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -323,6 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0) a.ws.part_lse[int64_t(s) * 128 + h] = -INFINITY;
         continue;
       }
+      const int L = seq_len_clamped(a, b);
       // queries of this piece: Qc half -> tensor memory, Qr half -> smem
       {
         const __nv_bfloat16* qrow = a.q_c + (int64_t(b) * 128 + h) * kDc + 256 * rank;
@@ -358,7 +383,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(BAR(B_Q_FULL));
       }
       float m_run = -INFINITY, l_run = 0.0f;
+      uint32_t vmask = 0;
       for (int j = pc.y; j < pc.z; ++j, ++t) {
+        if (((j - pc.y) & 31) == 0) vmask = valid_mask(a, b, j, pc.z);
         const uint32_t sb = t & 1u, par = (t >> 1) & 1u;
         if (!warp_ok(mbar_wait(BAR(B_S_FULL + sb), par, abort_flag, kWaitNs))) {
           ok = false;
@@ -383,12 +410,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t xrow = kSmX + sb * kX + uint32_t(h) * 256u;
-        const uint32_t prow = mapa(sb0 + xrow, peer);
+        {
+          const uint32_t prow = mapa(sb0 + xrow, peer);
+          const uint32_t pbar = mapa(BAR(B_X_FULL + sb), peer);
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          st_cluster_v4(prow + ((uint32_t(q) ^ uint32_t(h & 15)) << 4), sv[4 * q], sv[4 * q + 1],
-                        sv[4 * q + 2], sv[4 * q + 3]);
-        mbar_arrive_remote(mapa(BAR(B_X_FULL + sb), peer));
+          for (int q = 0; q < 16; ++q)
+            st_async_v4(prow + ((uint32_t(q) ^ uint32_t(h & 15)) << 4), sv[4 * q],
+                        sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3], pbar);
+        }
         if (!warp_ok(mbar_wait<true>(BAR(B_X_FULL + sb), par, abort_flag, kWaitNs))) {
           ok = false;
           break;
@@ -401,15 +430,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           sv[4 * q + 2] += v.z;
           sv[4 * q + 3] += v.w;
         }
+        // this CTA's buffer sb is read: expect the exchange two tiles ahead and
+        // tell the peer it may send it
+        if (h == 0) mbar_arrive_expect_tx(BAR(B_X_FULL + sb), kX);
         mbar_arrive_remote(mapa(BAR(B_X_EMPTY + sb), peer));
 
-        const int nvalid = tile_tokens(a, b, j);
-        float mt = -INFINITY;
+        const int nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          sv[i] = (i < nvalid) ? sv[i] * c2 : -INFINITY;
-          mt = fmaxf(mt, sv[i]);
+        for (int i = 0; i < 64; ++i) sv[i] *= c2;
+        if (nvalid < 64) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) sv[i] = (i < nvalid) ? sv[i] : -INFINITY;
         }
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mx8[k] = fmaxf(fmaxf(fmaxf(sv[8 * k], sv[8 * k + 1]), fmaxf(sv[8 * k + 2], sv[8 * k + 3])),
+                         fmaxf(fmaxf(sv[8 * k + 4], sv[8 * k + 5]), fmaxf(sv[8 * k + 6], sv[8 * k + 7])));
+        }
+        const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const bool need = mt > m_run + 8.0f;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mt : m_run;
@@ -437,15 +477,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m_run = m_new;
         }
         uint32_t pk[32];
-        float ls = 0.0f;
+        float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const float msub = (mt == -INFINITY) ? 0.0f : m_run;  // all masked: every p is 0
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = (mt == -INFINITY) ? 0.0f : exp2f(sv[2 * i] - m_run);
-          const float p1 = (mt == -INFINITY) ? 0.0f : exp2f(sv[2 * i + 1] - m_run);
-          const __half2 hp = __floats2half2_rn(p0, p1);
-          ls += __low2float(hp) + __high2float(hp);
-          pk[i] = *reinterpret_cast<const uint32_t*>(&hp);
+          const float p0 = ex2_approx(sv[2 * i] - msub);
+          const float p1 = ex2_approx(sv[2 * i + 1] - msub);
+          ls4[i & 3] += p0 + p1;
+          pk[i] = pack_half2(p0, p1);
         }
+        const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         l_run += ls;
         tmem_st32(tbase + lane_base + kColS + 64 * sb, pk);
         tmem_wait_st();
@@ -483,15 +524,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
       const int4 pc = a.ws.pieces[s];
+      const int L = seq_len_clamped(a, pc.x);
+      uint32_t vmask = 0;
       for (int j = pc.y; j < pc.z; ++j, ++t) {
-        const uint32_t st = t & 1u, kb = t & 1u, par = (t >> 1) & 1u;
-        bool got = mbar_wait(BAR(B_STAGE_FULL + st), par, abort_flag, kWaitNs);
-        got = got && mbar_wait(BAR(B_K_EMPTY + kb), par ^ 1u, abort_flag, kWaitNs);
+        if (((j - pc.y) & 31) == 0) vmask = valid_mask(a, pc.x, j, pc.z);
+        const uint32_t st = t % kStages, kb = t & 1u;
+        bool got = mbar_wait(BAR(B_STAGE_FULL + st), (t / kStages) & 1u, abort_flag, kWaitNs);
+        got = got && mbar_wait(BAR(B_K_EMPTY + kb), ((t >> 1) & 1u) ^ 1u, abort_flag, kWaitNs);
         if (!warp_ok(got)) {
           ok = false;
           break;
         }
-        const int nvalid = tile_tokens(a, pc.x, j);
+        const int nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
         const unsigned char* stg = sm + kSmStage + st * kStage;
         unsigned char* kt = sm + kSmK + kb * kKTile;
         // content: 4 groups x 64 tokens x 4 segments of 16 channels

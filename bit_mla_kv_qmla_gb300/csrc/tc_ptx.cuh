@@ -132,6 +132,24 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float a, float b, 
                : "memory");
 }
 
+// Asynchronous store into another CTA's shared memory: the bytes count
+// toward the transaction count of the mbarrier `cluster_bar` (in the
+// destination CTA), whose phase completes once they have all landed.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(caddr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+      : "memory");
+}
+// 2^x with the hardware approximation (relative error about 2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- TMEM
 // Warp-wide: allocate `ncols` (power of two >= 32) columns, address -> *dst.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
