@@ -32,16 +32,10 @@
 
 #include <cfloat>
 
-#include "plan.cuh"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace qmla {
-namespace {
-
-using namespace ptx;
-
-constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
-
+namespace tc {
 // ---------------------------------------------------------------- planner
 // One warp writes the split plan: merge table, piece descriptors per slot
 // and the slot range of each worker.
@@ -83,6 +77,19 @@ __global__ void __launch_bounds__(32) plan_kernel(DecodeArgs a) {
   }
 }
 
+}  // namespace tc
+
+// The planner kernel is defined once, here, for both tensor-core decodes.
+cudaError_t launch_plan(const DecodeArgs& a, cudaStream_t stream) {
+  tc::plan_kernel<<<1, 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+namespace {
+
+using namespace ptx;
+using namespace tc;
+
 // ---------------------------------------------------------------- layout
 constexpr int kThreads = 448;
 constexpr int kMmaWarp = 1;
@@ -114,70 +121,6 @@ enum : uint32_t {
   B_STAGE_FULL = 0, B_STAGE_EMPTY = 4, B_K_FULL = 8, B_K_EMPTY = 10, B_S_FULL = 12,
   B_P_FULL = 14, B_PV_DONE = 16, B_X_FULL = 18, B_X_EMPTY = 20, B_Q_FULL = 22, B_DRAIN = 23
 };
-
-__device__ __forceinline__ bool wait_noabort(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitNs) return false;
-  return true;
-}
-// All lanes of the warp agree on the outcome of a wait, so that the warp stays
-// converged for the warp-synchronous tensor-memory instructions that follow.
-__device__ __forceinline__ bool warp_ok(bool v) { return __all_sync(0xffffffffu, v); }
-
-// Four pairs of binary16 values (channels 2k, 2k+1) from 8 INT4 codes packed
-// even-low / odd-high: x = code * s + z (exact on the quantizer's grid).
-__device__ __forceinline__ void dq_int4(uint32_t w, __half2 s2, __half2 z2, uint32_t* out) {
-  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t v = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
-    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), magic);
-    h = __hfma2(h, s2, z2);
-    out[k] = *reinterpret_cast<uint32_t*>(&h);
-  }
-}
-// Eight pairs from 16 INT2 codes.
-__device__ __forceinline__ void dq_int2(uint32_t w, __half2 s2, __half2 z2, uint32_t* out) {
-  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t v = ((w >> (2 * k)) & 0x00030003u) | 0x64006400u;
-    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), magic);
-    h = __hfma2(h, s2, z2);
-    out[k] = *reinterpret_cast<uint32_t*>(&h);
-  }
-}
-__device__ __forceinline__ void split_sz(uint32_t sz, __half2& s2, __half2& z2) {
-  const __half s = __ushort_as_half(uint16_t(sz & 0xffffu));
-  const __half z = __ushort_as_half(uint16_t(sz >> 16));
-  s2 = __halves2half2(s, s);
-  z2 = __halves2half2(z, z);
-}
-// 16 channels (8 words) into row `row` of an SW128 [rows][64 fp16] region,
-// logical 16-byte granules 2*seg and 2*seg+1.
-__device__ __forceinline__ void st_row16(unsigned char* region, int row, int seg,
-                                         const uint32_t* v) {
-  unsigned char* r = region + (row >> 3) * 1024 + (row & 7) * 128;
-  *reinterpret_cast<uint4*>(r + (((2 * seg) ^ (row & 7)) << 4)) =
-      make_uint4(v[0], v[1], v[2], v[3]);
-  *reinterpret_cast<uint4*>(r + (((2 * seg + 1) ^ (row & 7)) << 4)) =
-      make_uint4(v[4], v[5], v[6], v[7]);
-}
-
-// Validity of blocks j0 .. j0+31 of sequence b as a bit mask (bit k: block
-// j0+k exists in the piece and its id lies inside the pool).  One coalesced
-// load per warp for 32 tiles keeps global-memory latency out of the per-tile
-// path.  Called by a full warp.
-__device__ __forceinline__ uint32_t valid_mask(const DecodeArgs& a, int b, int j0, int j1) {
-  const int j = j0 + int(threadIdx.x & 31);
-  bool ok = false;
-  if (j < j1) {
-    const int32_t blk = a.block_table[int64_t(b) * a.max_blocks_per_seq + j];
-    ok = blk >= 0 && blk < a.num_blocks;
-  }
-  return __ballot_sync(0xffffffffu, ok);
-}
 
 // ---------------------------------------------------------------- kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -593,24 +536,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int tc_workers(int sms, int heads) {
-  (void)heads;
-  return sms / 2 > 0 ? sms / 2 : 1;
-}
-
-bool tc_supported(int fmt, int heads) {
-  return heads == 128 && (fmt == QMLA_C4R4 || fmt == QMLA_C2R4);
-}
-
-cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
-  plan_kernel<<<1, 32, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+cudaError_t launch_decode_tc128(const DecodeArgs& a, cudaStream_t stream) {
+  cudaError_t e = launch_plan(a, stream);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(decode_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmDyn));
   if (e != cudaSuccess) return e;
   decode_tc128_kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(a);
   return cudaGetLastError();
+}
+
+int tc_workers(int sms, int heads) {
+  if (heads == 16) return sms > 0 ? sms : 1;
+  return sms / 2 > 0 ? sms / 2 : 1;
+}
+
+bool tc_supported(int fmt, int heads) {
+  return (heads == 128 || heads == 16) && (fmt == QMLA_C4R4 || fmt == QMLA_C2R4);
+}
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
+  return a.heads == 16 ? launch_decode_tc16(a, stream) : launch_decode_tc128(a, stream);
 }
 
 }  // namespace qmla
