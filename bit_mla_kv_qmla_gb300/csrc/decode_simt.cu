@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
 int simt_workers(int sms) { return 2 * sms; }
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream) {
+  static int smem_attr_done[kMaxDevices];
   const size_t smem = sizeof(SimtShared);
-  cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = ensure_smem_attr(decode_simt_kernel, int(smem), smem_attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(unsigned(a.workers), unsigned(a.heads / kHG));
   decode_simt_kernel<<<grid, kThreads, smem, stream>>>(a);

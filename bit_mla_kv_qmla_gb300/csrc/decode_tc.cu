@@ -214,16 +214,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16(128, 64, false, false);
       const uint32_t idesc_pv = idesc_f16(128, 256, false, true);
+      // operand descriptors; an offset advances the 16-byte address field
+      const uint64_t dKt = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
+      const uint64_t dCt = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
+      const uint64_t dQr = smem_desc(sb0 + kSmQr, 16, 1024, kSwizzle128B);
       uint32_t t = 0, piece = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t tt, bool first) {
         const uint32_t sb = tt & 1u;
-        const uint32_t kt = sb0 + kSmK + sb * kKTile;
 #pragma unroll
         for (uint32_t kk = 0; kk < 4; ++kk) {
           mma_ts(tbase + kColO, tbase + kColS + 64 * sb + 8 * kk,
-                 smem_desc(kt + kk * 2048, kChunk, 1024, kSwizzle128B), idesc_pv,
-                 (first && kk == 0) ? 0u : 1u);
+                 dCt + ((sb * kKTile + kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
         }
         mma_commit(BAR(B_PV_DONE + sb));
         mma_commit(BAR(B_K_EMPTY + sb));
@@ -242,17 +244,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t kt = sb0 + kSmK + sb * kKTile;
+          const uint64_t dk = dKt + ((sb * kKTile) >> 4);
           const uint32_t d = tbase + kColS + 64 * sb;
 #pragma unroll
           for (uint32_t kc = 0; kc < 16; ++kc)
-            mma_ts(d, tbase + kColQ + 8 * kc,
-                   smem_desc(kt + (kc >> 2) * kChunk + (kc & 3) * 32, 16, 1024, kSwizzle128B),
+            mma_ts(d, tbase + kColQ + 8 * kc, dk + (((kc >> 2) * kChunk + (kc & 3) * 32) >> 4),
                    idesc_qk, kc > 0 ? 1u : 0u);
 #pragma unroll
           for (uint32_t kr = 0; kr < 2; ++kr)
-            mma_ss(d, smem_desc(sb0 + kSmQr + kr * 32, 16, 1024, kSwizzle128B),
-                   smem_desc(kt + 4 * kChunk + kr * 32, 16, 1024, kSwizzle128B), idesc_qk, 1u);
+            mma_ss(d, dQr + ((kr * 32) >> 4), dk + ((4 * kChunk + kr * 32) >> 4), idesc_qk, 1u);
           mma_commit(BAR(B_S_FULL + sb));
           if (j > pc.y) {
             const uint32_t tp = t - 1;
@@ -481,25 +481,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
         const unsigned char* stg = sm + kSmStage + st * kStage;
         unsigned char* kt = sm + kSmK + kb * kKTile;
-        // content: 4 groups x 64 tokens x 4 segments of 16 channels
-#pragma unroll 1
-        for (int it = dt; it < 1024; it += kDequantThreads) {
-          const int g = it >> 8, tt = (it >> 2) & 63, seg = it & 3;
-          uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (tt < nvalid) {
+        // content: thread dt owns token tt and 16-channel segment seg of each of
+        // the 4 groups of this half; unconditional loads, invalid tokens zeroed
+        {
+          const int tt = (dt >> 2) & 63, seg = dt & 3;
+          const bool valid = tt < nvalid;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
             __half2 s2, z2;
             split_sz(*reinterpret_cast<const uint32_t*>(stg + G.sz_off + (g * 64 + tt) * 4), s2,
                      z2);
+            uint32_t v[8];
             if (G.cbits == 4) {
               const uint2 w = *reinterpret_cast<const uint2*>(stg + g * 2048 + tt * 32 + seg * 8);
               dq_int4(w.x, s2, z2, v);
               dq_int4(w.y, s2, z2, v + 4);
             } else {
-              dq_int2(*reinterpret_cast<const uint32_t*>(stg + g * 1024 + tt * 16 + seg * 4), s2,
-                      z2, v);
+              dq_int2(*reinterpret_cast<const uint32_t*>(stg + g * 1024 + tt * 16 + seg * 4), s2, z2,
+                      v);
             }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = valid ? v[k] : 0u;
+            st_row16(kt + g * kChunk, tt, seg, v);
           }
-          st_row16(kt + g * kChunk, tt, seg, v);
         }
         // RoPE: 64 tokens x 2 segments of 16 channels (INT4)
         if (dt < 128) {
@@ -537,10 +541,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_decode_tc128(const DecodeArgs& a, cudaStream_t stream) {
+  static int smem_attr_done[kMaxDevices];
   cudaError_t e = launch_plan(a, stream);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(kSmDyn));
+  e = ensure_smem_attr(decode_tc128_kernel, int(kSmDyn), smem_attr_done);
   if (e != cudaSuccess) return e;
   decode_tc128_kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(a);
   return cudaGetLastError();

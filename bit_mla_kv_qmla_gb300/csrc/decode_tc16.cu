@@ -40,7 +40,7 @@ constexpr int kDequantThreads = 256;
 constexpr int kH = 16;                                 // heads
 
 constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kColS = 0, kColO = 64;              // S^T 16 cols, O^T 4 x 16 cols
+constexpr uint32_t kColS = 0, kColO = 64;              // S^T 4 x 16 (partial sums), O^T 4 x 16
 
 constexpr uint32_t kChunk = 16384;                     // [128 tok][64 ch] fp16 SW128
 constexpr uint32_t kSmK = 0;                           // 8 content chunks + RoPE chunk
@@ -150,7 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16(128, kH, false, false);
       const uint32_t idesc_pv = idesc_f16(128, kH, true, false);
-      const uint32_t sK = sb0 + kSmK, sQ = sb0 + kSmQ, sP = sb0 + kSmP;
+      // operand descriptors; an offset inside the tile advances the 16-byte
+      // address field (shared memory < 256 KB: no carry out of the field)
+      const uint64_t dK = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
+      const uint64_t dQ = smem_desc(sb0 + kSmQ, 16, 1024, kSwizzle128B);
+      const uint64_t dC = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
+      const uint64_t dP = smem_desc(sb0 + kSmP, 16, 1024, kSwizzle128B);
       uint32_t t = 0, piece = 0;
       bool ok = true;
       for (int s = wr.x; ok && s <= wr.y; ++s) {
@@ -164,12 +169,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
             break;
           }
           tc_fence_after();
-#pragma unroll 4
-          for (uint32_t ks = 0; ks < 36; ++ks) {
-            const uint32_t c = ks >> 2, koff = (ks & 3u) * 32u;
-            mma_ss(tbase + kColS, smem_desc(sK + c * kChunk + koff, 16, 1024, kSwizzle128B),
-                   smem_desc(sQ + c * 2048 + koff, 16, 1024, kSwizzle128B), idesc_qk,
-                   ks > 0 ? 1u : 0u);
+          // four independent partial sums over k-steps 9p..9p+8, issued round
+          // robin: chained MMAs into one accumulator serialize on its latency
+#pragma unroll
+          for (uint32_t i = 0; i < 9; ++i) {
+#pragma unroll
+            for (uint32_t p = 0; p < 4; ++p) {
+              const uint32_t ks = 9 * p + i, c = ks >> 2, koff = (ks & 3u) * 32u;
+              mma_ss(tbase + kColS + kH * p, dK + ((c * kChunk + koff) >> 4),
+                     dQ + ((c * 2048 + koff) >> 4), idesc_qk, i > 0 ? 1u : 0u);
+            }
           }
           mma_commit(BAR(B_S_FULL));
           if (!mbar_wait(BAR(B_P_FULL), t & 1u, abort_flag, kWaitNs)) {
@@ -178,14 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
           }
           tc_fence_after();
           const bool first = (jt == pc.y);
-#pragma unroll 1
-          for (uint32_t mk = 0; mk < 4; ++mk) {
 #pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks)
-              mma_ss(tbase + kColO + kH * mk,
-                     smem_desc(sK + 2 * mk * kChunk + ks * 2048, kChunk, 1024, kSwizzle128B),
-                     smem_desc(sP + (ks >> 2) * 2048 + (ks & 3u) * 32u, 16, 1024, kSwizzle128B),
-                     idesc_pv, (first && ks == 0) ? 0u : 1u);
+          for (uint32_t ks = 0; ks < 8; ++ks) {
+#pragma unroll
+            for (uint32_t mk = 0; mk < 4; ++mk)
+              mma_ss(tbase + kColO + kH * mk, dC + ((2 * mk * kChunk + ks * 2048) >> 4),
+                     dP + (((ks >> 2) * 2048 + (ks & 3u) * 32u) >> 4), idesc_pv,
+                     (first && ks == 0) ? 0u : 1u);
           }
           mma_commit(BAR(B_PV_DONE));
           mma_commit(BAR(B_K_EMPTY));
@@ -254,11 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         tc_fence_after();
         float sv[kH];
         {
-          uint32_t q16[16];
-          tmem_ld16(tbase + lane_base + kColS, q16);
+          uint32_t q0[32], q1[32];
+          tmem_ld32(tbase + lane_base + kColS, q0);
+          tmem_ld32(tbase + lane_base + kColS + 32, q1);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < kH; ++h) sv[h] = row_ok ? __uint_as_float(q16[h]) * c2 : -INFINITY;
+          for (int h = 0; h < kH; ++h) {
+            const float v = (__uint_as_float(q0[h]) + __uint_as_float(q0[16 + h])) +
+                            (__uint_as_float(q1[h]) + __uint_as_float(q1[16 + h]));
+            sv[h] = row_ok ? v * c2 : -INFINITY;
+          }
         }
         // per-head maximum over the 128 token rows
         float wm[kH];
@@ -387,46 +400,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
             }
             nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
           }
-          // 8 content groups x 64 tokens x 4 segments, then RoPE 64 tokens x 4 segments
-#pragma unroll 1
-          for (int it = dt; it < 2304; it += kDequantThreads) {
-            uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            int chunk, tt, seg;
-            if (it < 2048) {
-              const int g = it >> 8;
-              tt = (it >> 2) & 63;
-              seg = it & 3;
-              chunk = g;
-              if (tt < nvalid) {
-                const unsigned char* half = stg + (g >> 2) * G.half;
-                const int gi = g & 3;
-                __half2 s2, z2;
-                split_sz(*reinterpret_cast<const uint32_t*>(half + G.sz_off + (gi * 64 + tt) * 4),
-                         s2, z2);
-                if (G.cbits == 4) {
-                  const uint2 w = *reinterpret_cast<const uint2*>(half + gi * 2048 + tt * 32 + seg * 8);
-                  dq_int4(w.x, s2, z2, v);
-                  dq_int4(w.y, s2, z2, v + 4);
-                } else {
-                  dq_int2(*reinterpret_cast<const uint32_t*>(half + gi * 1024 + tt * 16 + seg * 4),
-                          s2, z2, v);
-                }
-              }
-            } else {
-              const int q = it - 2048;
-              tt = q >> 2;
-              seg = q & 3;
-              chunk = 8;
-              if (tt < nvalid) {
-                __half2 s2, z2;
-                split_sz(*reinterpret_cast<const uint32_t*>(stg + G.rope_sz_off + tt * 4), s2, z2);
-                const uint2 w = *reinterpret_cast<const uint2*>(stg + (seg >> 1) * G.half +
-                                                                G.rope_off + tt * 16 + (seg & 1) * 8);
+          // thread dt owns token tt and 16-channel segment seg of every group
+          // (8 tokens x 4 segments per warp: conflict-free reads and writes);
+          // loads are unconditional and invalid tokens are zeroed by a select,
+          // so the unrolled groups' loads can all be in flight together
+          {
+            const int tt = (dt >> 2) & 63, seg = dt & 3;
+            const bool valid = tt < nvalid;
+            const int row = 64 * bi + tt;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const unsigned char* half = stg + (g >> 2) * G.half;
+              const int gi = g & 3;
+              __half2 s2, z2;
+              split_sz(*reinterpret_cast<const uint32_t*>(half + G.sz_off + (gi * 64 + tt) * 4), s2,
+                       z2);
+              uint32_t v[8];
+              if (G.cbits == 4) {
+                const uint2 w = *reinterpret_cast<const uint2*>(half + gi * 2048 + tt * 32 + seg * 8);
                 dq_int4(w.x, s2, z2, v);
                 dq_int4(w.y, s2, z2, v + 4);
+              } else {
+                dq_int2(*reinterpret_cast<const uint32_t*>(half + gi * 1024 + tt * 16 + seg * 4), s2,
+                        z2, v);
               }
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[k] = valid ? v[k] : 0u;
+              st_row16(sm + kSmK + g * kChunk, row, seg, v);
             }
-            st_row16(sm + kSmK + chunk * kChunk, 64 * bi + tt, seg, v);
+            // RoPE (INT4): the same token and segment of the 64 RoPE channels
+            {
+              __half2 s2, z2;
+              split_sz(*reinterpret_cast<const uint32_t*>(stg + G.rope_sz_off + tt * 4), s2, z2);
+              const uint2 w = *reinterpret_cast<const uint2*>(stg + (seg >> 1) * G.half + G.rope_off +
+                                                              tt * 16 + (seg & 1) * 8);
+              uint32_t v[8];
+              dq_int4(w.x, s2, z2, v);
+              dq_int4(w.y, s2, z2, v + 4);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[k] = valid ? v[k] : 0u;
+              st_row16(sm + kSmK + 8 * kChunk, row, seg, v);
+            }
           }
           if (present) {
             __syncwarp();
@@ -454,10 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
 }  // namespace
 
 cudaError_t launch_decode_tc16(const DecodeArgs& a, cudaStream_t stream) {
+  static int smem_attr_done[kMaxDevices];
   cudaError_t e = launch_plan(a, stream);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_tc16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(kSmDyn));
+  e = ensure_smem_attr(decode_tc16_kernel, int(kSmDyn), smem_attr_done);
   if (e != cudaSuccess) return e;
   decode_tc16_kernel<<<dim3(unsigned(a.workers)), kThreads, kSmDyn, stream>>>(a);
   return cudaGetLastError();

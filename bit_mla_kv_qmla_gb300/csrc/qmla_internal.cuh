@@ -115,6 +115,21 @@ struct DecodeArgs {
   int32_t* status;
 };
 
+// Raise a kernel's dynamic shared-memory limit once per device (the
+// attribute is per function and device; repeating it costs a runtime call on
+// every launch).  `done` is the caller's own per-device record for this kernel.
+constexpr int kMaxDevices = 64;
+template <typename K>
+inline cudaError_t ensure_smem_attr(K* kernel, int bytes, int (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = bytes;
+  return e;
+}
+
 // Kernel launchers (each defined next to its kernel).  They return a
 // cudaError_t from the launch.
 cudaError_t launch_append(int fmt, uint8_t* blocks, int64_t num_blocks, const int32_t* table,
