@@ -179,13 +179,37 @@ def run_ours(args, rank, world, device):
     for k in range(args.warmup):
         step(k)
     torch.cuda.synchronize(device)
+
+    # The step (append + decode, all in the library's kernels) is captured once
+    # per cache copy into a CUDA graph and replayed, so the timed region
+    # measures the device work, not Python/ctypes launch overhead (the e2e
+    # figure below keeps that overhead).  Decode-only graphs time the decode
+    # call for the roofline.
+    use_graph = not args.no_graph
+    if use_graph:
+        g_step, g_dec = [], []
+        for i in range(copies):
+            gs = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gs):
+                if n_app:
+                    caches[i].append(new_lat[i, :, :n_app], new_rope[i, :, :n_app])
+                decs[i](qc, qr, w.scale)
+            g_step.append(gs)
+            gd = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gd):
+                decs[i](qc, qr, w.scale)
+            g_dec.append(gd)
+        torch.cuda.synchronize(device)
+        # capturing records the work without running it; replay each step
+        # graph once so every copy has run a graph step before timing
+        for i in range(copies):
+            g_step[i].replay()
+        torch.cuda.synchronize(device)
     lens_at = [list(c.seq_lens.cpu().tolist()) for c in caches]
 
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
     time.sleep(0.15)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -193,16 +217,22 @@ def run_ours(args, rank, world, device):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     tokens = 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     t0.record(stream)
-    for k in range(args.warmup, total_steps):
+    for k in range(args.steps):
         i = k % copies
         if n_app:
-            caches[i].append(new_lat[i, :, :n_app], new_rope[i, :, :n_app])
             lens_at[i] = [L + n_app for L in lens_at[i]]
-        e = ev[k - args.warmup]
-        e[0].record(stream)
-        decs[i](qc, qr, w.scale)
-        e[1].record(stream)
+        if use_graph:
+            g_step[i].replay()
+        else:
+            if n_app:
+                caches[i].append(new_lat[i, :, :n_app], new_rope[i, :, :n_app])
+            e = ev[k]
+            e[0].record(stream)
+            decs[i](qc, qr, w.scale)
+            e[1].record(stream)
         tokens += sum(lens_at[i])
     t1.record(stream)
     torch.cuda.synchronize(device)
@@ -210,6 +240,13 @@ def run_ours(args, rank, world, device):
         dist.barrier()
     clocks = sampler.stop()
     elapsed = t0.elapsed_time(t1) / 1e3
+    if use_graph:  # decode-only replays, one event pair each, L2 rotated by the copies
+        for k in range(args.steps):
+            e = ev[k]
+            e[0].record(stream)
+            g_dec[k % copies].replay()
+            e[1].record(stream)
+        torch.cuda.synchronize(device)
     t_dec = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
     for c in caches:
         assert c.status.item() == 0, "device status flag set during the benchmark"
@@ -267,7 +304,9 @@ def run_ours(args, rank, world, device):
     res = {"tokens": tokens, "elapsed": elapsed, "t_dec": t_dec, "roofline": roof,
            "dtype": "f16" if tc else "f32",
            "clocks": clocks, "e2e": e2e, "workload": w, "copies": copies,
-           "cache_bytes": cache_bytes, "launches": args.steps * ((1 if n_app else 0) + 2)}
+           "cache_bytes": cache_bytes,
+           "launches": args.steps * ((1 if n_app else 0) + (3 if tc else 2)),
+           "graph": use_graph}
     return res
 
 
@@ -388,6 +427,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-also", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch each step's calls eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -454,6 +495,8 @@ def main():
         "dtype": res["dtype"], "data": "synthetic (seeded, bit_mla_kv_qmla_gb300/workloads.py)",
         "config": {"workload": w.name, "format": w.fmt, "batch": w.batch, "heads": w.heads,
                    "seq_len": w.seq_len, "append_per_step": max(1, w.n_append),
+                   "launch": ("CUDA graph replay of each step's library calls" if res["graph"]
+                              else "eager library calls"),
                    "l2": (f"rotating {res['copies']} cache copies of "
                           f"{res['cache_bytes'] / 1e6:.0f} MB (> L2 129 MB in total)"
                           if res["copies"] > 1 else "cache larger than L2")},
