@@ -35,8 +35,8 @@ L2_BYTES = 129 * 2**20
 TOKEN_BYTES = {"C4R4": 324, "C2R4": 196, "BF16": 1152}
 FLOP_PER_TOKEN_HEAD = 2 * (576 + 512)
 IO_BYTES_PER_HEAD = 576 * 2 + 512 * 2 + 4  # q in, O out, LSE out
-DECODE_SOURCES = ["decode_tc.cu", "decode_simt.cu", "plan.cuh", "qmla_internal.cuh",
-                  "combine.cu"]
+DECODE_SOURCES = ["decode_tc.cu", "decode_tc16.cu", "decode_simt.cu", "plan.cuh",
+                  "qmla_internal.cuh", "tc_common.cuh", "tc_ptx.cuh", "combine.cu"]
 
 
 def peaks():
