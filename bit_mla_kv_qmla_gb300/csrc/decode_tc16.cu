@@ -5,22 +5,42 @@
 // both halves of the MLA cache" (flowchart node "Low-bit kernel: dequant
 // inside attention") for the small-head-count case.  With 16 heads the
 // product is too thin for heads on the MMA's M dimension (M >= 64), so the
-// tokens go there instead:
-//   QK : S^T[128 tok x 16 heads] = K[128 tok x 576] (A, smem, K-major)
+// 128 tokens of a tile (two cache blocks) go there instead:
+//   QK : S^T[128 tok x 16 heads] = K[128 tok x 576] (A, tensor memory)
 //                                 x Q^T              (B, smem, 16 rows)
-//   PV : O^T[512 ch x 16 heads] += C^T[512 ch x 128 tok] (A, the same smem
-//        tile read MN-major, 4 slices of 128 channels) x P^T (B, smem)
-// One CTA per SM; tensor memory holds S^T (16 columns) and O^T (4 x 16).
-// The softmax runs over tokens, i.e. across the 128 lanes of S^T: per-head
-// maxima are reduced with warp shuffles and across the four softmax warps
-// through shared memory; row sums are kept per lane and reduced once per
-// piece.  Rescaling of O^T is lazy (only when a maximum grows by more than 8
-// in log2 units).
+//   PV : O^T[512 ch x 16 heads] += C^T[512 ch x 128 tok] (A, smem, read
+//        MN-major in 4 slices of 128 channels) x P^T (B, smem)
+// The dequantization warps write every binary16 value twice: into tensor
+// memory (lane = token) for QK and into a swizzled shared-memory tile for PV.
+// K in tensor memory keeps half of the MMA operand traffic out of shared
+// memory and lets QK of a tile chase its dequantization: a tile is two work
+// items (half 0 of both blocks: content channels 0-255 and RoPE 0-31; half 1:
+// content 256-511 and RoPE 32-63), each with full/empty barriers.  The
+// shared-memory content tile of a half goes to one of three 64 KB groups, so
+// the dequantization of a tile's first half overlaps the softmax and P.V
+// products of the previous tile.  The packed codes need no staging in shared
+// memory: the dequantization threads load them straight from global memory
+// (32 bytes per token and group in one 256-bit load), one half-tile ahead of
+// use, and a producer warp keeps the next few tiles' blocks streaming into L2
+// with bulk prefetches.
 //
-// Warp roles (14 warps): 0 bulk-copy producer (whole blocks), 1 MMA issuer,
-// 2-5 softmax (thread = token lane), 6-13 dequantization.  Binary16 operands
-// (exact on the quantizer's grid), binary32 accumulation.  Waits are bounded;
-// a timeout raises an abort flag and QMLA_STATUS_TIMEOUT.
+// At M=128, N=16 an MMA costs a roughly fixed ~50 cycles to issue, so the
+// MMA count (36 QK + 32 PV per tile) and every wait/commit around them set the
+// pace.  Two converged warps issue them, one for QK and one for P.V (an
+// elected lane issues each instruction), with few synchronization points per
+// tile.
+//
+// The softmax runs over tokens, i.e. across the 128 lanes of S^T.  A tile
+// first checks, with one OR-barrier, whether any score exceeds the running
+// maximum by more than 8 (log2 units); only then are per-head maxima reduced
+// and O^T rescaled (lazy rescaling).  Row sums are kept per lane and reduced
+// once per piece.
+//
+// Warp roles (15 warps): 0 L2 prefetcher, 1 QK issuer, 2 P.V issuer,
+// 3-6 softmax (thread = token lane), 7-14 dequantization (two warps per lane
+// quarter).  Binary16 operands (exact on the quantizer's grid), binary32
+// accumulation.  Waits are bounded; a timeout raises an abort flag and
+// QMLA_STATUS_TIMEOUT.
 
 #include <cfloat>
 
@@ -32,34 +52,110 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-constexpr int kThreads = 448;
-constexpr int kMmaWarp = 1;
-constexpr int kSoftmaxWarp0 = 2;
-constexpr int kDequantWarp0 = 6;
-constexpr int kDequantThreads = 256;
-constexpr int kH = 16;                                 // heads
+constexpr int kThreads = 480;
+constexpr int kQkWarp = 1;
+constexpr int kPvWarp = 2;
+constexpr int kSoftmaxWarp0 = 3;
+constexpr int kDequantWarp0 = 7;
+constexpr int kH = 16;  // heads
 
-constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kColS = 0, kColO = 64;              // S^T 4 x 16 (partial sums), O^T 4 x 16
+// tensor memory columns (32-bit); K holds binary16 pairs (channel 2j, 2j+1)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColK = 0;       // content chunk c (64 channels) at 32c
+constexpr uint32_t kColRope = 256;  // RoPE channels, 32 columns
+constexpr uint32_t kColS = 288;     // S^T: 4 partial sums x 16
+constexpr uint32_t kColO = 352;     // O^T: 4 slices of 128 channels x 16
 
-constexpr uint32_t kChunk = 16384;                     // [128 tok][64 ch] fp16 SW128
-constexpr uint32_t kSmK = 0;                           // 8 content chunks + RoPE chunk
-constexpr uint32_t kSmQ = kSmK + 9 * kChunk;           // 9 x [16 heads][128 B]
-constexpr uint32_t kSmP = kSmQ + 9 * 2048;             // 2 x [16 heads][128 B] (P^T)
-constexpr uint32_t kSmStage = kSmP + 2 * 2048;         // 2 x one whole block
-constexpr uint32_t kStage = 20736;                     // largest block (C4R4)
-constexpr uint32_t kSmRed = kSmStage + 2 * kStage;     // [4 warps][16] max, [4][16] sum
+// shared memory
+constexpr uint32_t kChunk = 16384;                   // [128 tok][64 ch] fp16, SW128
+constexpr uint32_t kGroup = 4 * kChunk;              // content tile of one half
+constexpr uint32_t kSmV = 0;                         // 3 groups
+constexpr uint32_t kSmQ = kSmV + 3 * kGroup;         // 9 x [16 heads][128 B]
+constexpr uint32_t kSmP = kSmQ + 9 * 2048;           // 2 buffers x 2 x [16 heads][128 B]
+constexpr uint32_t kSmRed = kSmP + 2 * 4096;         // [4][16] max, [4][16] sum
 constexpr uint32_t kSmBar = kSmRed + 512;
-constexpr uint32_t kNumBars = 11;
+enum : uint32_t {
+  B_K_FULL = 0,                  // [2] per half
+  B_K_EMPTY = B_K_FULL + 2,      // [2]
+  B_V_EMPTY = B_K_EMPTY + 2,     // [3] per content group
+  B_S_FULL = B_V_EMPTY + 3,
+  B_S_EMPTY = B_S_FULL + 1,
+  B_P_FULL = B_S_EMPTY + 1,      // [2] per P buffer
+  B_PV_DONE = B_P_FULL + 2,
+  B_Q_FULL = B_PV_DONE + 1,
+  B_DRAIN_QK = B_Q_FULL + 1,
+  B_DRAIN_PV = B_DRAIN_QK + 1,
+  kNumBars = B_DRAIN_PV + 1
+};
 constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
-constexpr uint32_t kSmBytes = kSmAbort + 12;
+constexpr uint32_t kSmProgress = kSmAbort + 4;       // tiles dequantized (prefetch pacing)
+constexpr uint32_t kSmBytes = kSmProgress + 8;
 constexpr uint32_t kSmDyn = kSmBytes + 1024;
+static_assert(kSmDyn <= 232448, "shared memory budget");
+constexpr uint32_t kPrefetchTiles = 4;               // L2 prefetch distance
 
-enum : uint32_t {
-  B_STAGE_FULL = 0, B_STAGE_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 5, B_S_FULL = 6,
-  B_P_FULL = 7, B_PV_DONE = 8, B_Q_FULL = 9, B_DRAIN = 10
+// Packed codes of one half-tile for one dequantization thread: two content
+// groups (codes and scale/zero) and 16 RoPE channels (codes, scale/zero).
+struct HalfCodes {
+  uint32_t c0[8], c1[8];
+  uint32_t sz0, sz1, rope0, rope1, rsz;
 };
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_nc_v4(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_nc_v2(const void* p, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
+}
+__device__ __forceinline__ uint32_t ld_nc_b32(const void* p) {
+  uint32_t a;
+  asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(a) : "l"(p));
+  return a;
+}
+// Issue the loads of half h for token tt and column half dw of block `blk`
+// (nullptr: nothing to load; the scale/zero words read as 0, which turns
+// every dequantized value into +0 whatever the codes hold).
+__device__ __forceinline__ void load_half(HalfCodes& L, const uint8_t* blk, const Geom& G, int h,
+                                          int dw, int tt) {
+  if (blk == nullptr) {
+    L.sz0 = L.sz1 = L.rsz = 0u;
+    return;
+  }
+  const uint8_t* half = blk + h * G.half;
+  const int g0 = 2 * dw;
+  if (G.cbits == 4) {
+    ld_nc_v8(half + g0 * 2048 + tt * 32, L.c0);
+    ld_nc_v8(half + (g0 + 1) * 2048 + tt * 32, L.c1);
+  } else {
+    ld_nc_v4(half + g0 * 1024 + tt * 16, L.c0);
+    ld_nc_v4(half + (g0 + 1) * 1024 + tt * 16, L.c1);
+  }
+  L.sz0 = ld_nc_b32(half + G.sz_off + (g0 * 64 + tt) * 4);
+  L.sz1 = ld_nc_b32(half + G.sz_off + ((g0 + 1) * 64 + tt) * 4);
+  ld_nc_v2(half + G.rope_off + tt * 16 + dw * 8, L.rope0, L.rope1);
+  L.rsz = ld_nc_b32(blk + G.rope_sz_off + tt * 4);
+}
+// 64 binary16 values (32 words, channel pairs) of one content group.
+__device__ __forceinline__ void dq_group(const Geom& G, const uint32_t* c, uint32_t sz,
+                                         uint32_t* v) {
+  __half2 s2, z2;
+  split_sz(sz, s2, z2);
+  if (G.cbits == 4) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) dq_int4(c[w], s2, z2, v + 4 * w);
+  } else {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) dq_int2(c[w], s2, z2, v + 8 * w);
+  }
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -73,9 +169,10 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // offset from the shared array itself, so that every access stays a
+  // shared-memory access
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb0 = smem_u32(sm);
   auto BAR = [&](uint32_t i) { return sb0 + kSmBar + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmAbort);
@@ -83,22 +180,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   const int worker = blockIdx.x;
   const Geom G = geom(a.fmt);
 
+  volatile int* progress = reinterpret_cast<volatile int*>(sm + kSmProgress);
   if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < 2; ++i) {
-      mbar_init(BAR(B_STAGE_FULL + i), 1);
-      mbar_init(BAR(B_STAGE_EMPTY + i), kDequantThreads / 32);
+    for (uint32_t h = 0; h < 2; ++h) {
+      mbar_init(BAR(B_K_FULL + h), 8);  // every dequantization warp
+      mbar_init(BAR(B_K_EMPTY + h), 1);
+      mbar_init(BAR(B_P_FULL + h), 128);
     }
-    mbar_init(BAR(B_K_FULL), kDequantThreads / 32);
-    mbar_init(BAR(B_K_EMPTY), 1);
+    for (uint32_t g = 0; g < 3; ++g) mbar_init(BAR(B_V_EMPTY + g), 1);
     mbar_init(BAR(B_S_FULL), 1);
-    mbar_init(BAR(B_P_FULL), 128);
+    mbar_init(BAR(B_S_EMPTY), 4);  // every softmax warp
     mbar_init(BAR(B_PV_DONE), 1);
     mbar_init(BAR(B_Q_FULL), 128);
-    mbar_init(BAR(B_DRAIN), 1);
+    mbar_init(BAR(B_DRAIN_QK), 1);
+    mbar_init(BAR(B_DRAIN_PV), 1);
     *abort_flag = 0;
+    *progress = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tmem_alloc(sb0 + kSmTslot, kTmemCols);
     tmem_relinquish();
   }
@@ -109,8 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   const int2 wr = a.ws.wrange[worker];
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    uint32_t u = 0;  // block counter
+    // ------------------------------------------------------------ L2 prefetch
+    // keeps the blocks of the next kPrefetchTiles tiles streaming into L2
+    // ahead of the dequantization warps' loads (a hint: nothing waits on it)
+    uint32_t t = 0;
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
       const int4 pc = a.ws.pieces[s];
@@ -118,90 +220,117 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         const int n = min(32, pc.z - jb);
         const int32_t my_blk =
             (lane < n) ? a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + jb + lane] : -1;
-        for (int k = 0; k < n; ++k, ++u) {
-          const int32_t blk = __shfl_sync(0xffffffffu, my_blk, k);
-          bool got = true;
-          if (lane == 0) {
-            const uint32_t st = u & 1u, par = (u >> 1) & 1u;
-            got = mbar_wait(BAR(B_STAGE_EMPTY + st), par ^ 1u, abort_flag, kWaitNs);
-            if (got) {
-              if (blk >= 0 && blk < a.num_blocks) {
-                mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), uint32_t(G.block));
-                bulk_g2s(sb0 + kSmStage + st * kStage, a.blocks + int64_t(blk) * G.block,
-                         uint32_t(G.block), BAR(B_STAGE_FULL + st));
-              } else {
-                set_status(a.status, QMLA_STATUS_BAD_BLOCK);
-                mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), 0u);
+        for (int k = 0; ok && k < n; k += 2, ++t) {
+          if (lane == 0 && t >= kPrefetchTiles) {
+            const uint64_t t0 = globaltimer();
+            // polls sparsely: this warp shares its scheduler with working warps
+            while (*progress < int(t - kPrefetchTiles) + 1 && !*abort_flag) {
+              __nanosleep(500);
+              if (globaltimer() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                break;
               }
             }
           }
-          if (!warp_ok(got)) {
-            ok = false;
-            break;
-          }
+          ok = warp_ok(!*abort_flag);
+          const int32_t blk = __shfl_sync(0xffffffffu, my_blk, min(k + (lane & 1), 31));
+          if (lane < 2 && k + lane < n && blk >= 0 && blk < a.num_blocks)
+            bulk_prefetch_l2(a.blocks + int64_t(blk) * G.block, uint32_t(G.block));
+          __syncwarp();
         }
       }
     }
-    if (lane == 0)
-      for (uint32_t v = (u >= 2 ? u - 2 : 0); v < u; ++v)
-        wait_noabort(BAR(B_STAGE_FULL + (v & 1u)), (v >> 1) & 1u);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16(128, kH, false, false);
-      const uint32_t idesc_pv = idesc_f16(128, kH, true, false);
-      // operand descriptors; an offset inside the tile advances the 16-byte
-      // address field (shared memory < 256 KB: no carry out of the field)
-      const uint64_t dK = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
-      const uint64_t dQ = smem_desc(sb0 + kSmQ, 16, 1024, kSwizzle128B);
-      const uint64_t dC = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
-      const uint64_t dP = smem_desc(sb0 + kSmP, 16, 1024, kSwizzle128B);
-      uint32_t t = 0, piece = 0;
-      bool ok = true;
-      for (int s = wr.x; ok && s <= wr.y; ++s) {
-        const int4 pc = a.ws.pieces[s];
-        if (pc.z <= pc.y) continue;
-        if (!mbar_wait(BAR(B_Q_FULL), piece & 1u, abort_flag, kWaitNs)) break;
-        ++piece;
-        for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
-          if (!mbar_wait(BAR(B_K_FULL), t & 1u, abort_flag, kWaitNs)) {
+  } else if (warp == kQkWarp) {
+    // ------------------------------------------------------------ QK^T issuer
+    // k-step ks of every content chunk accumulates into partial sum ks, so the
+    // four products of a chunk are independent of one another; RoPE k-steps
+    // 0-1 come with half 0, 2-3 with half 1
+    const uint32_t idesc = idesc_f16(128, kH, false, false);
+    // operand descriptor; an offset inside the tile advances the 16-byte
+    // address field (shared memory < 256 KB: no carry out of the field)
+    const uint64_t dQ = smem_desc(sb0 + kSmQ, 16, 1024, kSwizzle128B);
+    uint32_t t = 0, piece = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      if (pc.z <= pc.y) continue;
+      if (!warp_ok(mbar_wait(BAR(B_Q_FULL), piece & 1u, abort_flag, kWaitNs))) break;
+      ++piece;
+      for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
+        // the softmax has read the previous tile's scores
+        if (!warp_ok(mbar_wait(BAR(B_S_EMPTY), (t & 1u) ^ 1u, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (uint32_t h = 0; h < 2; ++h) {
+          if (!warp_ok(mbar_wait(BAR(B_K_FULL + h), t & 1u, abort_flag, kWaitNs))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // four independent partial sums over k-steps 9p..9p+8, issued round
-          // robin: chained MMAs into one accumulator serialize on its latency
 #pragma unroll
-          for (uint32_t i = 0; i < 9; ++i) {
+          for (uint32_t cc = 0; cc < 4; ++cc) {
+            const uint32_t c = 4 * h + cc;
 #pragma unroll
-            for (uint32_t p = 0; p < 4; ++p) {
-              const uint32_t ks = 9 * p + i, c = ks >> 2, koff = (ks & 3u) * 32u;
-              mma_ss(tbase + kColS + kH * p, dK + ((c * kChunk + koff) >> 4),
-                     dQ + ((c * 2048 + koff) >> 4), idesc_qk, i > 0 ? 1u : 0u);
-            }
+            for (uint32_t ks = 0; ks < 4; ++ks)
+              mma_ts_warp(tbase + kColS + kH * ks, tbase + kColK + 32 * c + 8 * ks,
+                          dQ + ((c * 2048 + 32 * ks) >> 4), idesc, c > 0 ? 1u : 0u);
           }
-          mma_commit(BAR(B_S_FULL));
-          if (!mbar_wait(BAR(B_P_FULL), t & 1u, abort_flag, kWaitNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const bool first = (jt == pc.y);
+#pragma unroll
+          for (uint32_t ks = 2 * h; ks < 2 * h + 2; ++ks)
+            mma_ts_warp(tbase + kColS + kH * ks, tbase + kColRope + 8 * ks,
+                        dQ + ((8 * 2048 + 32 * ks) >> 4), idesc, 1u);
+          mma_commit_warp(BAR(B_K_EMPTY + h));
+        }
+        if (!ok) break;
+        mma_commit_warp(BAR(B_S_FULL));
+      }
+    }
+    mma_commit_warp(BAR(B_DRAIN_QK));
+    if (lane == 0) wait_noabort(BAR(B_DRAIN_QK), 0);
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ P.V issuer
+    // in two halves of the channels; half hv of tile t reads content group
+    // (2t + hv) mod 3 and frees it for the dequantization when done
+    const uint32_t idesc = idesc_f16(128, kH, true, false);
+    const uint64_t dV = smem_desc(sb0 + kSmV, kChunk, 1024, kSwizzle128B);
+    const uint64_t dP = smem_desc(sb0 + kSmP, 16, 1024, kSwizzle128B);
+    uint32_t t = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
+        if (!warp_ok(mbar_wait(BAR(B_P_FULL + (t & 1u)), (t >> 1) & 1u, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool first = (jt == pc.y);
+        const uint32_t pbuf = (t & 1u) * 4096u;
+#pragma unroll
+        for (uint32_t hv = 0; hv < 2; ++hv) {
+          const uint32_t grp = (2 * t + hv) % 3;
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) {
 #pragma unroll
-            for (uint32_t mk = 0; mk < 4; ++mk)
-              mma_ss(tbase + kColO + kH * mk, dC + ((2 * mk * kChunk + ks * 2048) >> 4),
-                     dP + (((ks >> 2) * 2048 + (ks & 3u) * 32u) >> 4), idesc_pv,
-                     (first && ks == 0) ? 0u : 1u);
+            for (uint32_t m2 = 0; m2 < 2; ++m2) {
+              const uint32_t mk = 2 * hv + m2;
+              mma_ss_warp(tbase + kColO + kH * mk,
+                          dV + ((grp * kGroup + 2 * m2 * kChunk + ks * 2048) >> 4),
+                          dP + ((pbuf + (ks >> 2) * 2048 + (ks & 3u) * 32u) >> 4), idesc,
+                          (first && ks == 0) ? 0u : 1u);
+            }
           }
-          mma_commit(BAR(B_PV_DONE));
-          mma_commit(BAR(B_K_EMPTY));
+          mma_commit_warp(BAR(B_V_EMPTY + grp));
         }
+        mma_commit_warp(BAR(B_PV_DONE));
       }
-      mma_commit(BAR(B_DRAIN));
-      wait_noabort(BAR(B_DRAIN), 0);
     }
+    mma_commit_warp(BAR(B_DRAIN_PV));
+    if (lane == 0) wait_noabort(BAR(B_DRAIN_PV), 0);
+    __syncwarp();
   } else if (warp >= kSoftmaxWarp0 && warp < kDequantWarp0) {
     // ------------------------------------------------------------ softmax
     const uint32_t quad = uint32_t(warp & 3);
@@ -224,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
       }
       const int L = seq_len_clamped(a, b);
       // Q^T of this piece: 16 heads x 576 channels, binary16, SW128 K-major
+      // (the QK products of the previous piece completed before its epilogue)
       for (int i = threadIdx.x - kSoftmaxWarp0 * 32; i < kH * 72; i += 128) {
         const int h = i / 72, sgm = i % 72;  // 8-channel segment
         const __nv_bfloat16* src =
@@ -255,17 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         const int bi = r >> 6, jj = jt + bi;
         const bool blk_ok = jj < pc.z && ((vmask >> ((jj - pc.y) & 31)) & 1u);
         const bool row_ok = blk_ok && (r & 63) < min(kT, L - jj * kT);
-        if (!warp_ok(mbar_wait(BAR(B_S_FULL), t & 1u, abort_flag, kWaitNs))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // scores of tile t; the P.V products of tile t-1 are complete before
+        // O^T is rescaled or the P buffer of tile t-2 is rewritten
+        bool got = warp_ok(mbar_wait(BAR(B_S_FULL), t & 1u, abort_flag, kWaitNs));
+        if (got && t > 0)
+          got = warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs));
         float sv[kH];
-        {
+#pragma unroll
+        for (int h = 0; h < kH; ++h) sv[h] = -INFINITY;
+        if (got) {
+          tc_fence_after();
           uint32_t q0[32], q1[32];
           tmem_ld32(tbase + lane_base + kColS, q0);
           tmem_ld32(tbase + lane_base + kColS + 32, q1);
           tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_S_EMPTY));
 #pragma unroll
           for (int h = 0; h < kH; ++h) {
             const float v = (__uint_as_float(q0[h]) + __uint_as_float(q0[16 + h])) +
@@ -273,43 +409,50 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
             sv[h] = row_ok ? v * c2 : -INFINITY;
           }
         }
-        // per-head maximum over the 128 token rows
-        float wm[kH];
+        // lazy rescale: the per-head maxima are only reduced when some score
+        // exceeds the maximum in use by more than 8; every thread then takes
+        // the same decisions.  All four warps take the same barriers whatever
+        // their waits returned: a failed wait forces the rare path, which
+        // checks for it.
+        bool over = !got;
 #pragma unroll
-        for (int h = 0; h < kH; ++h) wm[h] = warp_max(sv[h]);
-        if (lane == 0) {
+        for (int h = 0; h < kH; ++h) over |= sv[h] > m_used[h] + 8.0f;
+        if (named_bar_or(1, 128, over)) {
+          if (named_bar_or(1, 128, !got)) {
+            ok = false;
+            break;
+          }
+          float wm[kH];
 #pragma unroll
-          for (int h = 0; h < kH; h += 4)
-            *reinterpret_cast<float4*>(red_max + sw * kH + h) =
-                make_float4(wm[h], wm[h + 1], wm[h + 2], wm[h + 3]);
-        }
-        named_bar_sync(1, 128);
-        float mt[kH];
+          for (int h = 0; h < kH; ++h) wm[h] = warp_max(sv[h]);
+          if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < kH; h += 4) {
-          const float4 v0 = *reinterpret_cast<const float4*>(red_max + 0 * kH + h);
-          const float4 v1 = *reinterpret_cast<const float4*>(red_max + 1 * kH + h);
-          const float4 v2 = *reinterpret_cast<const float4*>(red_max + 2 * kH + h);
-          const float4 v3 = *reinterpret_cast<const float4*>(red_max + 3 * kH + h);
-          mt[h] = fmaxf(fmaxf(v0.x, v1.x), fmaxf(v2.x, v3.x));
-          mt[h + 1] = fmaxf(fmaxf(v0.y, v1.y), fmaxf(v2.y, v3.y));
-          mt[h + 2] = fmaxf(fmaxf(v0.z, v1.z), fmaxf(v2.z, v3.z));
-          mt[h + 3] = fmaxf(fmaxf(v0.w, v1.w), fmaxf(v2.w, v3.w));
-        }
-        // lazy rescale: identical decisions in every thread
-        bool any = false;
-        float alpha[kH];
+            for (int h = 0; h < kH; h += 4)
+              *reinterpret_cast<float4*>(red_max + sw * kH + h) =
+                  make_float4(wm[h], wm[h + 1], wm[h + 2], wm[h + 3]);
+          }
+          named_bar_sync(1, 128);
+          float alpha[kH];
 #pragma unroll
-        for (int h = 0; h < kH; ++h) {
-          const bool need = mt[h] > m_used[h] + 8.0f;
-          alpha[h] = need ? ex2_approx(m_used[h] - mt[h]) : 1.0f;
-          if (need) m_used[h] = mt[h];
-          any |= need;
-        }
-        if (any) {
+          for (int h = 0; h < kH; h += 4) {
+            const float4 v0 = *reinterpret_cast<const float4*>(red_max + 0 * kH + h);
+            const float4 v1 = *reinterpret_cast<const float4*>(red_max + 1 * kH + h);
+            const float4 v2 = *reinterpret_cast<const float4*>(red_max + 2 * kH + h);
+            const float4 v3 = *reinterpret_cast<const float4*>(red_max + 3 * kH + h);
+            const float mt[4] = {fmaxf(fmaxf(v0.x, v1.x), fmaxf(v2.x, v3.x)),
+                                 fmaxf(fmaxf(v0.y, v1.y), fmaxf(v2.y, v3.y)),
+                                 fmaxf(fmaxf(v0.z, v1.z), fmaxf(v2.z, v3.z)),
+                                 fmaxf(fmaxf(v0.w, v1.w), fmaxf(v2.w, v3.w))};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool need = mt[e] > m_used[h + e] + 8.0f;
+              alpha[h + e] = need ? ex2_approx(m_used[h + e] - mt[e]) : 1.0f;
+              if (need) m_used[h + e] = mt[e];
+            }
+          }
 #pragma unroll
           for (int h = 0; h < kH; ++h) l_part[h] *= alpha[h];
-          if (jt > pc.y) {  // O^T holds earlier tiles (P.V of the previous tile is done)
+          if (jt > pc.y) {  // O^T holds earlier tiles of this piece
 #pragma unroll 1
             for (uint32_t mk = 0; mk < 4; ++mk) {
               uint32_t o[16];
@@ -321,9 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
             }
             tmem_wait_st();
           }
+          // red_max is rewritten only after every softmax thread has passed
+          // this point: the next tile's scores need this tile's P first
         }
         // P^T[h][r] = 2^(s - m) as binary16 into the SW128 K-major B tile
-        unsigned char* preg = sm + kSmP + (r >> 6) * 2048;
+        unsigned char* preg = sm + kSmP + (t & 1u) * 4096u + (r >> 6) * 2048;
         const int tk = r & 63;
 #pragma unroll
         for (int h = 0; h < kH; ++h) {
@@ -335,11 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(BAR(B_P_FULL));
+        mbar_arrive(BAR(B_P_FULL + (t & 1u)));
       }
       if (!ok) break;
       // epilogue: row sums over the 128 lanes, normalized partial O, LSE
-      if (!warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs))) break;
+      const bool got = warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs));
+      if (named_bar_or(1, 128, !got)) break;
       tc_fence_after();
       float lsum[kH];
 #pragma unroll
@@ -374,84 +520,91 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant
-    const int dt = int(threadIdx.x) - kDequantWarp0 * 32;
-    uint32_t t = 0, u = 0;
+    // warp: lane quarter q (tensor-memory lanes 32q..32q+31 = token rows) and
+    // column half dw.  Rows 0-63 come from the tile's first block, 64-127 from
+    // its second.  For half h the warp dequantizes content groups 4h+2dw and
+    // 4h+2dw+1 and RoPE channels 32h+16dw .. 32h+16dw+15 of its tokens.  The
+    // loads of the next half-tile of the piece are issued before the current
+    // one is processed.
+    const int q = warp & 3, dw = (warp - kDequantWarp0) >> 2;
+    const int r = 32 * q + lane, bi = q >> 1, tt = r & 63;
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    const uint32_t vrow_off = uint32_t((r >> 3) * 1024 + (r & 7) * 128);  // row r of a chunk
+    const int sw7 = r & 7;
+    uint32_t t = 0;
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
       const int4 pc = a.ws.pieces[s];
+      if (pc.z <= pc.y) continue;
       const int L = seq_len_clamped(a, pc.x);
-      uint32_t vmask = 0;
-      for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
-        if (((jt - pc.y) & 31) == 0) vmask = valid_mask(a, pc.x, jt, pc.z);
-        if (!warp_ok(mbar_wait(BAR(B_K_EMPTY), (t & 1u) ^ 1u, abort_flag, kWaitNs))) {
-          ok = false;
-          break;
+      const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
+      // block of this thread's rows in the tile starting at jt (nullptr: none,
+      // or a bad block id), and the number of valid token rows in it
+      auto tile_block = [&](int jt, int& nvalid) -> const uint8_t* {
+        const int j = jt + bi;
+        nvalid = 0;
+        if (j >= pc.z) return nullptr;
+        const int32_t blk = btab[j];
+        if (blk < 0 || blk >= a.num_blocks) {
+          if (lane == 0) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
+          return nullptr;
         }
-        for (int bi = 0; bi < 2; ++bi) {
-          const int j = jt + bi;
-          const bool present = j < pc.z;
-          int nvalid = 0;
-          const unsigned char* stg = sm + kSmStage + (u & 1u) * kStage;
-          if (present) {
-            if (!warp_ok(mbar_wait(BAR(B_STAGE_FULL + (u & 1u)), (u >> 1) & 1u, abort_flag,
-                                   kWaitNs))) {
-              ok = false;
-              break;
-            }
-            nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
+        nvalid = min(kT, L - j * kT);
+        return a.blocks + int64_t(blk) * G.block;
+      };
+      int nv_cur;
+      const uint8_t* blk_cur = tile_block(pc.y, nv_cur);
+      HalfCodes cur, nxt;
+      load_half(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 0, dw, tt);
+      for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
+        int nv_next = 0;
+        const uint8_t* blk_next = (jt + 2 < pc.z) ? tile_block(jt + 2, nv_next) : nullptr;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          cur = nxt;
+          if (h == 0)
+            load_half(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 1, dw, tt);
+          else
+            load_half(nxt, (blk_next && tt < nv_next) ? blk_next : nullptr, G, 0, dw, tt);
+          const uint32_t n = 2 * t + uint32_t(h), grp = n % 3;
+          bool got = mbar_wait(BAR(B_K_EMPTY + h), (t & 1u) ^ 1u, abort_flag, kWaitNs);
+          got = got && mbar_wait(BAR(B_V_EMPTY + grp), ((n / 3) & 1u) ^ 1u, abort_flag, kWaitNs);
+          if (!warp_ok(got)) {
+            ok = false;
+            break;
           }
-          // thread dt owns token tt and 16-channel segment seg of every group
-          // (8 tokens x 4 segments per warp: conflict-free reads and writes);
-          // loads are unconditional and invalid tokens are zeroed by a select,
-          // so the unrolled groups' loads can all be in flight together
+          unsigned char* vgrp = sm + kSmV + grp * kGroup + vrow_off;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 4 * h + 2 * dw + cc;
+            uint32_t v[32];
+            dq_group(G, cc ? cur.c1 : cur.c0, cc ? cur.sz1 : cur.sz0, v);
+            tmem_st32(tbase + lane_base + kColK + 32 * c, v);
+            unsigned char* row = vgrp + (c & 3) * kChunk;
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              *reinterpret_cast<uint4*>(row + ((g ^ sw7) << 4)) =
+                  make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          }
           {
-            const int tt = (dt >> 2) & 63, seg = dt & 3;
-            const bool valid = tt < nvalid;
-            const int row = 64 * bi + tt;
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const unsigned char* half = stg + (g >> 2) * G.half;
-              const int gi = g & 3;
-              __half2 s2, z2;
-              split_sz(*reinterpret_cast<const uint32_t*>(half + G.sz_off + (gi * 64 + tt) * 4), s2,
-                       z2);
-              uint32_t v[8];
-              if (G.cbits == 4) {
-                const uint2 w = *reinterpret_cast<const uint2*>(half + gi * 2048 + tt * 32 + seg * 8);
-                dq_int4(w.x, s2, z2, v);
-                dq_int4(w.y, s2, z2, v + 4);
-              } else {
-                dq_int2(*reinterpret_cast<const uint32_t*>(half + gi * 1024 + tt * 16 + seg * 4), s2,
-                        z2, v);
-              }
-#pragma unroll
-              for (int k = 0; k < 8; ++k) v[k] = valid ? v[k] : 0u;
-              st_row16(sm + kSmK + g * kChunk, row, seg, v);
-            }
-            // RoPE (INT4): the same token and segment of the 64 RoPE channels
-            {
-              __half2 s2, z2;
-              split_sz(*reinterpret_cast<const uint32_t*>(stg + G.rope_sz_off + tt * 4), s2, z2);
-              const uint2 w = *reinterpret_cast<const uint2*>(stg + (seg >> 1) * G.half + G.rope_off +
-                                                              tt * 16 + (seg & 1) * 8);
-              uint32_t v[8];
-              dq_int4(w.x, s2, z2, v);
-              dq_int4(w.y, s2, z2, v + 4);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) v[k] = valid ? v[k] : 0u;
-              st_row16(sm + kSmK + 8 * kChunk, row, seg, v);
-            }
+            // RoPE channels 32h+16dw .. +15 (INT4)
+            __half2 s2, z2;
+            split_sz(cur.rsz, s2, z2);
+            uint32_t v[8];
+            dq_int4(cur.rope0, s2, z2, v);
+            dq_int4(cur.rope1, s2, z2, v + 4);
+            tmem_st8(tbase + lane_base + kColRope + 16 * h + 8 * dw, v);
           }
-          if (present) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_STAGE_EMPTY + (u & 1u)));
-            ++u;
-          }
+          tmem_wait_st();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_K_FULL + h));
         }
         if (!ok) break;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_K_FULL));
+        if (warp == kDequantWarp0 && lane == 0) *progress = int(t) + 1;
+        blk_cur = blk_next;
+        nv_cur = nv_next;
       }
     }
   }
@@ -459,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) set_status(a.status, QMLA_STATUS_TIMEOUT);
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
