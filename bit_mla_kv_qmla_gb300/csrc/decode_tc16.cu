@@ -21,8 +21,7 @@
 // products of the previous tile.  The packed codes need no staging in shared
 // memory: the dequantization threads load them straight from global memory
 // (32 bytes per token and group in one 256-bit load), one half-tile ahead of
-// use, and a producer warp keeps the next few tiles' blocks streaming into L2
-// with bulk prefetches.
+// use, with block ids fetched 32 blocks at a time well ahead.
 //
 // At M=128, N=16 an MMA costs a roughly fixed ~50 cycles to issue, so the
 // MMA count (36 QK + 32 PV per tile) and every wait/commit around them set the
@@ -36,9 +35,8 @@
 // and O^T rescaled (lazy rescaling).  Row sums are kept per lane and reduced
 // once per piece.
 //
-// Warp roles (15 warps): 0 L2 prefetcher, 1 QK issuer, 2 P.V issuer,
-// 3-6 softmax (thread = token lane), 7-14 dequantization (two warps per lane
-// quarter).  Binary16 operands (exact on the quantizer's grid), binary32
+// Warp roles (14 warps): 0 QK issuer, 1 P.V issuer, 2-5 softmax (thread =
+// token lane), 6-13 dequantization (two warps per lane quarter).  Binary16 operands (exact on the quantizer's grid), binary32
 // accumulation.  Waits are bounded; a timeout raises an abort flag and
 // QMLA_STATUS_TIMEOUT.
 
@@ -52,11 +50,11 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-constexpr int kThreads = 480;
-constexpr int kQkWarp = 1;
-constexpr int kPvWarp = 2;
-constexpr int kSoftmaxWarp0 = 3;
-constexpr int kDequantWarp0 = 7;
+constexpr int kThreads = 448;
+constexpr int kQkWarp = 0;
+constexpr int kPvWarp = 1;
+constexpr int kSoftmaxWarp0 = 2;
+constexpr int kDequantWarp0 = 6;
 constexpr int kH = 16;  // heads
 
 // tensor memory columns (32-bit); K holds binary16 pairs (channel 2j, 2j+1)
@@ -81,19 +79,17 @@ enum : uint32_t {
   B_S_FULL = B_V_EMPTY + 3,
   B_S_EMPTY = B_S_FULL + 1,
   B_P_FULL = B_S_EMPTY + 1,      // [2] per P buffer
-  B_PV_DONE = B_P_FULL + 2,
-  B_Q_FULL = B_PV_DONE + 1,
+  B_PV_DONE = B_P_FULL + 2,      // [2] per tile parity
+  B_Q_FULL = B_PV_DONE + 2,
   B_DRAIN_QK = B_Q_FULL + 1,
   B_DRAIN_PV = B_DRAIN_QK + 1,
   kNumBars = B_DRAIN_PV + 1
 };
 constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
-constexpr uint32_t kSmProgress = kSmAbort + 4;       // tiles dequantized (prefetch pacing)
-constexpr uint32_t kSmBytes = kSmProgress + 8;
+constexpr uint32_t kSmBytes = kSmAbort + 12;
 constexpr uint32_t kSmDyn = kSmBytes + 1024;
 static_assert(kSmDyn <= 232448, "shared memory budget");
-constexpr uint32_t kPrefetchTiles = 4;               // L2 prefetch distance
 
 // Packed codes of one half-tile for one dequantization thread: two content
 // groups (codes and scale/zero) and 16 RoPE channels (codes, scale/zero).
@@ -143,17 +139,18 @@ __device__ __forceinline__ void load_half(HalfCodes& L, const uint8_t* blk, cons
   ld_nc_v2(half + G.rope_off + tt * 16 + dw * 8, L.rope0, L.rope1);
   L.rsz = ld_nc_b32(blk + G.rope_sz_off + tt * 4);
 }
-// 64 binary16 values (32 words, channel pairs) of one content group.
-__device__ __forceinline__ void dq_group(const Geom& G, const uint32_t* c, uint32_t sz,
-                                         uint32_t* v) {
+// Channels 32*part .. 32*part+31 of one content group as 16 words of
+// binary16 pairs (channel 2k low, 2k+1 high).
+__device__ __forceinline__ void dq_group_part(const Geom& G, const uint32_t* c, uint32_t sz,
+                                              int part, uint32_t* v) {
   __half2 s2, z2;
   split_sz(sz, s2, z2);
   if (G.cbits == 4) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) dq_int4(c[w], s2, z2, v + 4 * w);
+    for (int w = 0; w < 4; ++w) dq_int4(c[4 * part + w], s2, z2, v + 4 * w);
   } else {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) dq_int2(c[w], s2, z2, v + 8 * w);
+    for (int w = 0; w < 2; ++w) dq_int2(c[2 * part + w], s2, z2, v + 8 * w);
   }
 }
 
@@ -180,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   const int worker = blockIdx.x;
   const Geom G = geom(a.fmt);
 
-  volatile int* progress = reinterpret_cast<volatile int*>(sm + kSmProgress);
   if (threadIdx.x == 0) {
     for (uint32_t h = 0; h < 2; ++h) {
       mbar_init(BAR(B_K_FULL + h), 8);  // every dequantization warp
@@ -190,12 +186,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     for (uint32_t g = 0; g < 3; ++g) mbar_init(BAR(B_V_EMPTY + g), 1);
     mbar_init(BAR(B_S_FULL), 1);
     mbar_init(BAR(B_S_EMPTY), 4);  // every softmax warp
-    mbar_init(BAR(B_PV_DONE), 1);
+    mbar_init(BAR(B_PV_DONE + 0), 1);
+    mbar_init(BAR(B_PV_DONE + 1), 1);
     mbar_init(BAR(B_Q_FULL), 128);
     mbar_init(BAR(B_DRAIN_QK), 1);
     mbar_init(BAR(B_DRAIN_PV), 1);
     *abort_flag = 0;
-    *progress = 0;
     fence_mbar_init();
   }
   if (warp == kQkWarp) {
@@ -208,39 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kSmTslot);
   const int2 wr = a.ws.wrange[worker];
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ L2 prefetch
-    // keeps the blocks of the next kPrefetchTiles tiles streaming into L2
-    // ahead of the dequantization warps' loads (a hint: nothing waits on it)
-    uint32_t t = 0;
-    bool ok = true;
-    for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
-      for (int jb = pc.y; ok && jb < pc.z; jb += 32) {
-        const int n = min(32, pc.z - jb);
-        const int32_t my_blk =
-            (lane < n) ? a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + jb + lane] : -1;
-        for (int k = 0; ok && k < n; k += 2, ++t) {
-          if (lane == 0 && t >= kPrefetchTiles) {
-            const uint64_t t0 = globaltimer();
-            // polls sparsely: this warp shares its scheduler with working warps
-            while (*progress < int(t - kPrefetchTiles) + 1 && !*abort_flag) {
-              __nanosleep(500);
-              if (globaltimer() - t0 > kWaitNs) {
-                *abort_flag = 1;
-                break;
-              }
-            }
-          }
-          ok = warp_ok(!*abort_flag);
-          const int32_t blk = __shfl_sync(0xffffffffu, my_blk, min(k + (lane & 1), 31));
-          if (lane < 2 && k + lane < n && blk >= 0 && blk < a.num_blocks)
-            bulk_prefetch_l2(a.blocks + int64_t(blk) * G.block, uint32_t(G.block));
-          __syncwarp();
-        }
-      }
-    }
-  } else if (warp == kQkWarp) {
+  if (warp == kQkWarp) {
     // ------------------------------------------------------------ QK^T issuer
     // k-step ks of every content chunk accumulates into partial sum ks, so the
     // four products of a chunk are independent of one another; RoPE k-steps
@@ -325,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
           }
           mma_commit_warp(BAR(B_V_EMPTY + grp));
         }
-        mma_commit_warp(BAR(B_PV_DONE));
+        mma_commit_warp(BAR(B_PV_DONE + (t & 1u)));
       }
     }
     mma_commit_warp(BAR(B_DRAIN_PV));
@@ -385,11 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         const int bi = r >> 6, jj = jt + bi;
         const bool blk_ok = jj < pc.z && ((vmask >> ((jj - pc.y) & 31)) & 1u);
         const bool row_ok = blk_ok && (r & 63) < min(kT, L - jj * kT);
-        // scores of tile t; the P.V products of tile t-1 are complete before
-        // O^T is rescaled or the P buffer of tile t-2 is rewritten
+        // scores of tile t; P buffer t&1 was last read by the P.V products of
+        // tile t-2 (PV_DONE[b] completes for tiles b, b+2, ...), so the
+        // softmax of tile t overlaps the P.V products of tile t-1
         bool got = warp_ok(mbar_wait(BAR(B_S_FULL), t & 1u, abort_flag, kWaitNs));
-        if (got && t > 0)
-          got = warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs));
+        if (got && t > 1)
+          got = warp_ok(mbar_wait(BAR(B_PV_DONE + (t & 1u)), ((t >> 1) & 1u) ^ 1u, abort_flag,
+                                  kWaitNs));
         float sv[kH];
 #pragma unroll
         for (int h = 0; h < kH; ++h) sv[h] = -INFINITY;
@@ -453,6 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
 #pragma unroll
           for (int h = 0; h < kH; ++h) l_part[h] *= alpha[h];
           if (jt > pc.y) {  // O^T holds earlier tiles of this piece
+            // the P.V products of tile t-1 must have landed in O^T first
+            // (uniform: every softmax thread is in this branch)
+            if (!warp_ok(mbar_wait(BAR(B_PV_DONE + ((t - 1) & 1u)), ((t - 1) >> 1) & 1u,
+                                   abort_flag, kWaitNs))) {
+              ok = false;  // abort raised: every role unwinds
+            }
 #pragma unroll 1
             for (uint32_t mk = 0; mk < 4; ++mk) {
               uint32_t o[16];
@@ -482,9 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         tc_fence_before();
         mbar_arrive(BAR(B_P_FULL + (t & 1u)));
       }
-      if (!ok) break;
+      // every softmax warp reaches this barrier (the loop is left together)
+      if (named_bar_or(1, 128, !ok)) {
+        ok = false;
+        break;
+      }
       // epilogue: row sums over the 128 lanes, normalized partial O, LSE
-      const bool got = warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs));
+      const bool got = warp_ok(mbar_wait(BAR(B_PV_DONE + ((t - 1) & 1u)), ((t - 1) >> 1) & 1u,
+                                         abort_flag, kWaitNs));
       if (named_bar_or(1, 128, !got)) break;
       tc_fence_after();
       float lsum[kH];
@@ -531,20 +508,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     const uint32_t vrow_off = uint32_t((r >> 3) * 1024 + (r & 7) * 128);  // row r of a chunk
     const int sw7 = r & 7;
-    uint32_t t = 0;
+    uint32_t t = 0;  // tiles of this worker before the current piece
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
       const int4 pc = a.ws.pieces[s];
       if (pc.z <= pc.y) continue;
       const int L = seq_len_clamped(a, pc.x);
       const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
+      // block ids of blocks jb0 .. jb0+63 of the piece, one per lane in two
+      // registers; the next 32 are loaded 16 tiles before they are needed, so
+      // no code load waits on a block-table load
+      int jb0 = pc.y;
+      int32_t ids_a = (jb0 + lane < pc.z) ? btab[jb0 + lane] : -1;
+      int32_t ids_b = (jb0 + 32 + lane < pc.z) ? btab[jb0 + 32 + lane] : -1;
       // block of this thread's rows in the tile starting at jt (nullptr: none,
       // or a bad block id), and the number of valid token rows in it
       auto tile_block = [&](int jt, int& nvalid) -> const uint8_t* {
-        const int j = jt + bi;
+        const int j = jt + bi, k = j - jb0;  // k < 64, the same in the whole warp
+        const int32_t va = __shfl_sync(0xffffffffu, ids_a, k & 31);
+        const int32_t vb = __shfl_sync(0xffffffffu, ids_b, k & 31);
         nvalid = 0;
         if (j >= pc.z) return nullptr;
-        const int32_t blk = btab[j];
+        const int32_t blk = k < 32 ? va : vb;
         if (blk < 0 || blk >= a.num_blocks) {
           if (lane == 0) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
           return nullptr;
@@ -557,8 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
       HalfCodes cur, nxt;
       load_half(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 0, dw, tt);
       for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
+        if (jt >= jb0 + 32) {
+          jb0 += 32;
+          ids_a = ids_b;
+          ids_b = (jb0 + 32 + lane < pc.z) ? btab[jb0 + 32 + lane] : -1;
+        }
         int nv_next = 0;
-        const uint8_t* blk_next = (jt + 2 < pc.z) ? tile_block(jt + 2, nv_next) : nullptr;
+        const uint8_t* blk_next = tile_block(jt + 2, nv_next);
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           cur = nxt;
@@ -566,9 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
             load_half(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 1, dw, tt);
           else
             load_half(nxt, (blk_next && tt < nv_next) ? blk_next : nullptr, G, 0, dw, tt);
-          const uint32_t n = 2 * t + uint32_t(h), grp = n % 3;
+          const uint32_t hn = 2 * t + uint32_t(h), grp = hn % 3;
           bool got = mbar_wait(BAR(B_K_EMPTY + h), (t & 1u) ^ 1u, abort_flag, kWaitNs);
-          got = got && mbar_wait(BAR(B_V_EMPTY + grp), ((n / 3) & 1u) ^ 1u, abort_flag, kWaitNs);
+          got = got && mbar_wait(BAR(B_V_EMPTY + grp), ((hn / 3) & 1u) ^ 1u, abort_flag, kWaitNs);
           if (!warp_ok(got)) {
             ok = false;
             break;
@@ -577,14 +567,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 4 * h + 2 * dw + cc;
-            uint32_t v[32];
-            dq_group(G, cc ? cur.c1 : cur.c0, cc ? cur.sz1 : cur.sz0, v);
-            tmem_st32(tbase + lane_base + kColK + 32 * c, v);
             unsigned char* row = vgrp + (c & 3) * kChunk;
+            // 32 channels (16 words) at a time
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-              *reinterpret_cast<uint4*>(row + ((g ^ sw7) << 4)) =
-                  make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            for (int part = 0; part < 2; ++part) {
+              uint32_t v[16];
+              dq_group_part(G, cc ? cur.c1 : cur.c0, cc ? cur.sz1 : cur.sz0, part, v);
+              tmem_st16(tbase + lane_base + kColK + 32 * c + 16 * part, v);
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<uint4*>(row + (((4 * part + g) ^ sw7) << 4)) =
+                    make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            }
           }
           {
             // RoPE channels 32h+16dw .. +15 (INT4)
@@ -602,7 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
           if (lane == 0) mbar_arrive(BAR(B_K_FULL + h));
         }
         if (!ok) break;
-        if (warp == kDequantWarp0 && lane == 0) *progress = int(t) + 1;
         blk_cur = blk_next;
         nv_cur = nv_next;
       }
