@@ -34,26 +34,35 @@ __device__ __forceinline__ float warp_max(float v) {
 // M = max(1, ceil((mx - Z*u) / (levels*u))) such that |Z| <= 2047 and
 // |Z + levels*M| <= 2047.  Every dequantized value (Z + c*M)*u is then exactly
 // a binary16 number, so the tensor cores multiply exactly the value the
-// quantizer defines.  Warp uniform; binary64 with explicitly rounded
-// intrinsics (the quotient for M is rounded up, so the bounds hold even when
-// it is inexact).
+// quantizer defines.  Warp uniform.  Every step is exact, so no rounding mode
+// matters and no binary64 division is needed: mn and mx (bfloat16 values)
+// scale by 2^-E exactly in binary64, Z is the floor of the scaled minimum,
+// N = mx/u - Z is an exact binary64 difference (N >= 0 since Z <= mn/u <=
+// mx/u), and M = ceil(N / levels) = ceil(ceil(N) / levels) is an integer
+// division.
 __device__ __forceinline__ void group_grid(float mn, float mx, int levels, float& s, float& z) {
-  const double d = __dsub_rd(double(mx), double(mn));
+  const double d = double(mx) - double(mn);  // exact
   int E = (d > 0.0) ? max(-24, ilogb(d) - 12) : -24;
   for (;; ++E) {
-    const double u = ldexp(1.0, E);
-    double Z = floor(__ddiv_rn(double(mn), u));
-    double M = ceil(__ddiv_ru(__dsub_ru(double(mx), __dmul_rn(Z, u)), __dmul_rn(double(levels), u)));
-    if (M < 1.0) M = 1.0;
-    const bool ok =
-        fabs(Z) <= 2047.0 && fabs(__dadd_rn(Z, __dmul_rn(double(levels), M))) <= 2047.0;
+    const double a_mn = ldexp(double(mn), -E), a_mx = ldexp(double(mx), -E);  // exact
+    const double Zd = floor(a_mn);
+    // |Z| and N beyond 2^40 fail the bounds below anyway; clamp before the
+    // integer conversion
+    const int64_t Z = int64_t(fmin(fmax(Zd, -1099511627776.0), 1099511627776.0));
+    const double N = fmin(a_mx - Zd, 1099511627776.0);  // exact below the clamp
+    int64_t M = (int64_t(ceil(N)) + levels - 1) / levels;
+    if (M < 1) M = 1;
+    const bool ok = (Z >= -2047 && Z <= 2047) && (Z + levels * M <= 2047);
     if (ok || E >= 5) {
+      int64_t Zc = Z, Mc = M;
       if (!ok) {  // outside the |x| < 32768 precondition: clamp into range
-        Z = fmin(2047.0, fmax(-2047.0, Z));
-        M = fmax(1.0, fmin(M, floor(__ddiv_rn(2047.0 - Z, double(levels)))));
+        Zc = Z < -2047 ? -2047 : (Z > 2047 ? 2047 : Z);
+        const int64_t mmax = (2047 - Zc) / levels;
+        Mc = M > mmax ? mmax : M;
+        if (Mc < 1) Mc = 1;
       }
-      z = float(__dmul_rn(Z, u));  // exact
-      s = float(__dmul_rn(M, u));  // exact
+      z = ldexpf(float(Zc), E);  // exact
+      s = ldexpf(float(Mc), E);  // exact
       return;
     }
   }
@@ -97,6 +106,14 @@ __global__ void __launch_bounds__(288) append_kernel(
   const int tok = blockIdx.x;  // b * n_new + i
   const int b = tok / n_new, i = tok % n_new;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the lane's two channels of this warp's group (issued first: independent
+  // of the block-table lookups below)
+  __nv_bfloat162 v;
+  if (warp < 8) {
+    v = reinterpret_cast<const __nv_bfloat162*>(latent + int64_t(tok) * kDc + warp * kG)[lane];
+  } else {
+    v = reinterpret_cast<const __nv_bfloat162*>(rope + int64_t(tok) * kDr)[lane];
+  }
   const int64_t pos = int64_t(positions[b]) + i;
   const int64_t jb = pos / kT;
   if (pos < 0 || jb >= max_blocks) {
@@ -112,13 +129,6 @@ __global__ void __launch_bounds__(288) append_kernel(
   const int slot = int(pos % kT);
   uint8_t* blk = blocks + int64_t(blk_id) * G.block;
 
-  // the lane's two channels of this warp's group
-  __nv_bfloat162 v;
-  if (warp < 8) {
-    v = reinterpret_cast<const __nv_bfloat162*>(latent + int64_t(tok) * kDc + warp * kG)[lane];
-  } else {
-    v = reinterpret_cast<const __nv_bfloat162*>(rope + int64_t(tok) * kDr)[lane];
-  }
 
   if (fmt == QMLA_BF16) {
     uint8_t* dst;

@@ -55,12 +55,18 @@ def test_append_full_size_sampled_bitexact(cfg, fmt, seqs):
 
 def _hard_tokens(n, seed):
     """Groups that stress the rounding rules: wide dynamic range, binary16
-    subnormal range, constant groups, single outliers, large magnitudes."""
+    subnormal range, values far below binary16, constant groups, single
+    outliers, large magnitudes."""
     g = torch.Generator().manual_seed(seed)
     lat = torch.randn(n, 512, generator=g)
     for t in range(n):
-        k = t % 6
-        if k == 1:
+        k = t % 8
+        if k == 6:
+            lat[t] *= 1e-30  # far below binary16: the grid bottoms out at 2^-24
+        elif k == 7:
+            lat[t] *= 1e-3
+            lat[t, 100] = -31000.0  # one huge outlier next to tiny values
+        elif k == 1:
             lat[t] *= 4e-6
         elif k == 2:
             lat[t, :64] = 1.25
