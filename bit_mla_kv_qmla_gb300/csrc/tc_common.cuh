@@ -23,27 +23,40 @@ __device__ __forceinline__ bool wait_noabort(uint32_t bar, uint32_t parity) {
 // converged for the warp-synchronous tensor-memory instructions that follow.
 __device__ __forceinline__ bool warp_ok(bool v) { return __all_sync(0xffffffffu, v); }
 
+// Binary16 of a small integer field without a shift: OR the field, sitting
+// at its bit position p inside each half-word, into the mantissa of 2^(10+p)
+// ("magic" exponent), so that the value reads 2^(10+p) + field; subtracting
+// 2^(10+p) leaves the field exactly.  Fields at bit 10 and above would reach
+// the exponent, so those come from the word shifted right once.
+__device__ __forceinline__ __half2 field_h2(uint32_t w, uint32_t mask, uint16_t magic) {
+  const uint32_t mm = uint32_t(magic) * 0x10001u;
+  const uint32_t v = (w & mask) | mm;
+  return __hsub2(*reinterpret_cast<const __half2*>(&v),
+                 *reinterpret_cast<const __half2*>(&mm));
+}
 // Four pairs of binary16 values (channels 2k, 2k+1) from 8 INT4 codes packed
 // even-low / odd-high: x = code * s + z (exact on the quantizer's grid).
 __device__ __forceinline__ void dq_int4(uint32_t w, __half2 s2, __half2 z2, uint32_t* out) {
-  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  const uint32_t w8 = w >> 8;
+  const __half2 c[4] = {field_h2(w, 0x000F000Fu, 0x6400), field_h2(w, 0x00F000F0u, 0x5400),
+                        field_h2(w8, 0x000F000Fu, 0x6400), field_h2(w8, 0x00F000F0u, 0x5400)};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t v = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
-    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), magic);
-    h = __hfma2(h, s2, z2);
-    out[k] = *reinterpret_cast<uint32_t*>(&h);
+    const __half2 h = __hfma2(c[k], s2, z2);
+    out[k] = *reinterpret_cast<const uint32_t*>(&h);
   }
 }
 // Eight pairs from 16 INT2 codes.
 __device__ __forceinline__ void dq_int2(uint32_t w, __half2 s2, __half2 z2, uint32_t* out) {
-  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  const uint32_t w10 = w >> 10;
+  const __half2 c[8] = {field_h2(w, 0x00030003u, 0x6400),   field_h2(w, 0x000C000Cu, 0x5C00),
+                        field_h2(w, 0x00300030u, 0x5400),   field_h2(w, 0x00C000C0u, 0x4C00),
+                        field_h2(w, 0x03000300u, 0x4400),   field_h2(w10, 0x00030003u, 0x6400),
+                        field_h2(w10, 0x000C000Cu, 0x5C00), field_h2(w10, 0x00300030u, 0x5400)};
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint32_t v = ((w >> (2 * k)) & 0x00030003u) | 0x64006400u;
-    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), magic);
-    h = __hfma2(h, s2, z2);
-    out[k] = *reinterpret_cast<uint32_t*>(&h);
+    const __half2 h = __hfma2(c[k], s2, z2);
+    out[k] = *reinterpret_cast<const uint32_t*>(&h);
   }
 }
 __device__ __forceinline__ void split_sz(uint32_t sz, __half2& s2, __half2& z2) {
