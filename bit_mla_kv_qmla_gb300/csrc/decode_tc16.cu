@@ -119,6 +119,7 @@ __device__ __forceinline__ uint32_t ld_nc_b32(const void* p) {
 // Issue the loads of half h for token tt and column half dw of block `blk`
 // (nullptr: nothing to load; the scale/zero words read as 0, which turns
 // every dequantized value into +0 whatever the codes hold).
+template <int kCBits>
 __device__ __forceinline__ void load_half(HalfCodes& L, const uint8_t* blk, const Geom& G, int h,
                                           int dw, int tt) {
   if (blk == nullptr) {
@@ -127,7 +128,7 @@ __device__ __forceinline__ void load_half(HalfCodes& L, const uint8_t* blk, cons
   }
   const uint8_t* half = blk + h * G.half;
   const int g0 = 2 * dw;
-  if (G.cbits == 4) {
+  if (kCBits == 4) {
     ld_nc_v8(half + g0 * 2048 + tt * 32, L.c0);
     ld_nc_v8(half + (g0 + 1) * 2048 + tt * 32, L.c1);
   } else {
@@ -141,11 +142,12 @@ __device__ __forceinline__ void load_half(HalfCodes& L, const uint8_t* blk, cons
 }
 // Channels 32*part .. 32*part+31 of one content group as 16 words of
 // binary16 pairs (channel 2k low, 2k+1 high).
-__device__ __forceinline__ void dq_group_part(const Geom& G, const uint32_t* c, uint32_t sz,
-                                              int part, uint32_t* v) {
+template <int kCBits>
+__device__ __forceinline__ void dq_group_part(const uint32_t* c, uint32_t sz, int part,
+                                              uint32_t* v) {
   __half2 s2, z2;
   split_sz(sz, s2, z2);
-  if (G.cbits == 4) {
+  if (kCBits == 4) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) dq_int4(c[4 * part + w], s2, z2, v + 4 * w);
   } else {
@@ -165,6 +167,7 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   return v;
 }
 
+template <int kCBits>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // offset from the shared array itself, so that every access stays a
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmAbort);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int worker = blockIdx.x;
-  const Geom G = geom(a.fmt);
+  const Geom G = geom(kCBits == 4 ? QMLA_C4R4 : QMLA_C2R4);
 
   if (threadIdx.x == 0) {
     for (uint32_t h = 0; h < 2; ++h) {
@@ -234,12 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
           }
           tc_fence_after();
 #pragma unroll
-          for (uint32_t cc = 0; cc < 4; ++cc) {
-            const uint32_t c = 4 * h + cc;
-#pragma unroll
-            for (uint32_t ks = 0; ks < 4; ++ks)
-              mma_ts_warp(tbase + kColS + kH * ks, tbase + kColK + 32 * c + 8 * ks,
-                          dQ + ((c * 2048 + 32 * ks) >> 4), idesc, c > 0 ? 1u : 0u);
+          for (uint32_t i = 0; i < 16; ++i) {  // content chunk 4h + i/4, k-step i%4
+            const uint32_t c = 4 * h + (i >> 2), ks = i & 3u;
+            mma_ts_warp(tbase + kColS + kH * ks, tbase + kColK + 32 * c + 8 * ks,
+                        dQ + ((c * 2048 + 32 * ks) >> 4), idesc, c > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (uint32_t ks = 2 * h; ks < 2 * h + 2; ++ks)
@@ -277,15 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         for (uint32_t hv = 0; hv < 2; ++hv) {
           const uint32_t grp = (2 * t + hv) % 3;
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) {
-#pragma unroll
-            for (uint32_t m2 = 0; m2 < 2; ++m2) {
-              const uint32_t mk = 2 * hv + m2;
-              mma_ss_warp(tbase + kColO + kH * mk,
-                          dV + ((grp * kGroup + 2 * m2 * kChunk + ks * 2048) >> 4),
-                          dP + ((pbuf + (ks >> 2) * 2048 + (ks & 3u) * 32u) >> 4), idesc,
-                          (first && ks == 0) ? 0u : 1u);
-            }
+          for (uint32_t i = 0; i < 16; ++i) {  // k-step i/2, slice 2hv + i%2
+            const uint32_t ks = i >> 1, m2 = i & 1u, mk = 2 * hv + m2;
+            mma_ss_warp(tbase + kColO + kH * mk,
+                        dV + ((grp * kGroup + 2 * m2 * kChunk + ks * 2048) >> 4),
+                        dP + ((pbuf + (ks >> 2) * 2048 + (ks & 3u) * 32u) >> 4), idesc,
+                        (first && ks == 0) ? 0u : 1u);
           }
           mma_commit_warp(BAR(B_V_EMPTY + grp));
         }
@@ -540,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
       int nv_cur;
       const uint8_t* blk_cur = tile_block(pc.y, nv_cur);
       HalfCodes cur, nxt;
-      load_half(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 0, dw, tt);
+      load_half<kCBits>(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 0, dw, tt);
       for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
         if (jt >= jb0 + 32) {
           jb0 += 32;
@@ -553,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
         for (int h = 0; h < 2; ++h) {
           cur = nxt;
           if (h == 0)
-            load_half(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 1, dw, tt);
+            load_half<kCBits>(nxt, (blk_cur && tt < nv_cur) ? blk_cur : nullptr, G, 1, dw, tt);
           else
-            load_half(nxt, (blk_next && tt < nv_next) ? blk_next : nullptr, G, 0, dw, tt);
+            load_half<kCBits>(nxt, (blk_next && tt < nv_next) ? blk_next : nullptr, G, 0, dw, tt);
           const uint32_t hn = 2 * t + uint32_t(h), grp = hn % 3;
           bool got = mbar_wait(BAR(B_K_EMPTY + h), (t & 1u) ^ 1u, abort_flag, kWaitNs);
           got = got && mbar_wait(BAR(B_V_EMPTY + grp), ((hn / 3) & 1u) ^ 1u, abort_flag, kWaitNs);
@@ -572,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
               uint32_t v[16];
-              dq_group_part(G, cc ? cur.c1 : cur.c0, cc ? cur.sz1 : cur.sz0, part, v);
+              dq_group_part<kCBits>(cc ? cur.c1 : cur.c0, cc ? cur.sz1 : cur.sz0, part, v);
               tmem_st16(tbase + lane_base + kColK + 32 * c + 16 * part, v);
 #pragma unroll
               for (int g = 0; g < 4; ++g)
@@ -614,12 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
 }  // namespace
 
 cudaError_t launch_decode_tc16(const DecodeArgs& a, cudaStream_t stream) {
-  static int smem_attr_done[kMaxDevices];
+  static int smem_attr_done[kMaxDevices], smem_attr_done2[kMaxDevices];
   cudaError_t e = launch_plan(a, stream);
   if (e != cudaSuccess) return e;
-  e = ensure_smem_attr(decode_tc16_kernel, int(kSmDyn), smem_attr_done);
+  auto kernel = (a.fmt == QMLA_C4R4) ? decode_tc16_kernel<4> : decode_tc16_kernel<2>;
+  e = ensure_smem_attr(kernel, int(kSmDyn), a.fmt == QMLA_C4R4 ? smem_attr_done : smem_attr_done2);
   if (e != cudaSuccess) return e;
-  decode_tc16_kernel<<<dim3(unsigned(a.workers)), kThreads, kSmDyn, stream>>>(a);
+  kernel<<<dim3(unsigned(a.workers)), kThreads, kSmDyn, stream>>>(a);
   return cudaGetLastError();
 }
 
