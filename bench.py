@@ -416,6 +416,21 @@ def cpu_baseline(cfg, fmt):
 
 # ---------------------------------------------------------------------------
 
+def aggregate_ranks(elapsed, tokens, world, device):
+    """Whole-job figures of a weak-scaling run: each rank decodes its own
+    batch (no data-path collective), so the job takes the slowest rank's time
+    and processes the sum of the ranks' tokens."""
+    if world <= 1:
+        return elapsed, tokens
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([tokens], dtype=torch.float64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -474,14 +489,7 @@ def main():
     __graft_entry__.build()
 
     res = run_ours(args, rank, world, device)
-    tok, el = float(res["tokens"]), float(res["elapsed"])
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([el], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        n = torch.tensor([tok], dtype=torch.float64, device=device)
-        dist.all_reduce(n, op=dist.ReduceOp.SUM)
-        el, tok = float(t.item()), float(n.item())
+    el, tok = aggregate_ranks(float(res["elapsed"]), float(res["tokens"]), world, device)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
