@@ -51,6 +51,32 @@ def test_decode_small_ragged(fmt, heads):
     assert torch.all(out[4] == 0) and torch.all(torch.isneginf(lse[4]))
 
 
+@pytest.mark.parametrize("fmt,heads", [("C4R4", 16), ("C2R4", 16), ("C4R4", 128)])
+def test_decode_large_batch_short_sequences(fmt, heads):
+    """More sequences than the 16-head kernel plans for itself (so its pieces
+    come from the planner kernel) and than workers, with ragged short lengths
+    and empty sequences: many workers see several sequences."""
+    w = W.Workload(f"batch_{fmt}_{heads}", fmt, 150, heads, 300, 0, "lognormal8", 0, 23)
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(0, 300, 150)]
+    lens[7] = 0
+    lens[8] = 1
+    lens[9] = 64
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cpu")
+    qc, qr = W.queries(w)
+    out, lse = Decoder(cache, heads, max(lens))(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    rows = [0, 7, 8, 9, 10, 77, 149]
+    table = cache.block_table.cpu().numpy()
+    for b in rows:
+        L = lens[b]
+        pool = oracle_pool_for_seq(w, b, L, table[b], cache.num_blocks, "cpu")
+        o, l = oracle.decode(W.FORMATS[w.fmt], pool, table[b:b + 1], np.array([L]),
+                             qc[b:b + 1].cpu(), qr[b:b + 1].cpu(), w.scale)
+        compare_rows(out[b:b + 1], lse[b:b + 1], o, l, f"{fmt} H{heads} seq {b}")
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_decode_tiny_workload(fmt):
     w = W.with_format(W.WORKLOADS[0], fmt)
