@@ -211,69 +211,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         wait_noabort(BAR(B_STAGE_FULL + u % kStages), (u / kStages) & 1u);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16(128, 64, false, false);
-      const uint32_t idesc_pv = idesc_f16(128, 256, false, true);
-      // operand descriptors; an offset advances the 16-byte address field
-      const uint64_t dKt = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
-      const uint64_t dCt = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
-      const uint64_t dQr = smem_desc(sb0 + kSmQr, 16, 1024, kSwizzle128B);
-      uint32_t t = 0, piece = 0;
-      bool ok = true;
-      auto issue_pv = [&](uint32_t tt, bool first) {
-        const uint32_t sb = tt & 1u;
+    // The whole warp runs the loop converged and an elected lane issues each
+    // instruction (single-lane issue behind waits and branches costs several
+    // times more per MMA).
+    const uint32_t idesc_qk = idesc_f16(128, 64, false, false);
+    const uint32_t idesc_pv = idesc_f16(128, 256, false, true);
+    // operand descriptors; an offset advances the 16-byte address field
+    const uint64_t dKt = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
+    const uint64_t dCt = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
+    const uint64_t dQr = smem_desc(sb0 + kSmQr, 16, 1024, kSwizzle128B);
+    uint32_t t = 0, piece = 0;
+    bool ok = true;
+    auto issue_pv = [&](uint32_t tt, bool first) {
+      const uint32_t sb = tt & 1u;
 #pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk) {
-          mma_ts(tbase + kColO, tbase + kColS + 64 * sb + 8 * kk,
-                 dCt + ((sb * kKTile + kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
+      for (uint32_t kk = 0; kk < 4; ++kk) {
+        mma_ts_warp(tbase + kColO, tbase + kColS + 64 * sb + 8 * kk,
+                    dCt + ((sb * kKTile + kk * 2048) >> 4), idesc_pv,
+                    (first && kk == 0) ? 0u : 1u);
+      }
+      mma_commit_warp(BAR(B_PV_DONE + sb));
+      mma_commit_warp(BAR(B_K_EMPTY + sb));
+    };
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      if (pc.z <= pc.y) continue;
+      if (!warp_ok(mbar_wait(BAR(B_Q_FULL), piece & 1u, abort_flag, kWaitNs))) break;
+      ++piece;
+      tc_fence_after();
+      for (int j = pc.y; j < pc.z; ++j, ++t) {
+        const uint32_t sb = t & 1u, par = (t >> 1) & 1u;
+        bool got = mbar_wait(BAR(B_K_FULL + sb), par, abort_flag, kWaitNs);
+        got = got && (t < 2 || mbar_wait(BAR(B_PV_DONE + sb), par ^ 1u, abort_flag, kWaitNs));
+        if (!warp_ok(got)) {
+          ok = false;
+          break;
         }
-        mma_commit(BAR(B_PV_DONE + sb));
-        mma_commit(BAR(B_K_EMPTY + sb));
-      };
-      for (int s = wr.x; ok && s <= wr.y; ++s) {
-        const int4 pc = a.ws.pieces[s];
-        if (pc.z <= pc.y) continue;
-        if (!mbar_wait(BAR(B_Q_FULL), piece & 1u, abort_flag, kWaitNs)) break;
-        ++piece;
         tc_fence_after();
-        for (int j = pc.y; j < pc.z; ++j, ++t) {
-          const uint32_t sb = t & 1u, par = (t >> 1) & 1u;
-          if (!mbar_wait(BAR(B_K_FULL + sb), par, abort_flag, kWaitNs) ||
-              (t >= 2 && !mbar_wait(BAR(B_PV_DONE + sb), par ^ 1u, abort_flag, kWaitNs))) {
+        const uint64_t dk = dKt + ((sb * kKTile) >> 4);
+        const uint32_t d = tbase + kColS + 64 * sb;
+#pragma unroll
+        for (uint32_t kc = 0; kc < 16; ++kc)
+          mma_ts_warp(d, tbase + kColQ + 8 * kc, dk + (((kc >> 2) * kChunk + (kc & 3) * 32) >> 4),
+                      idesc_qk, kc > 0 ? 1u : 0u);
+#pragma unroll
+        for (uint32_t kr = 0; kr < 2; ++kr)
+          mma_ss_warp(d, dQr + ((kr * 32) >> 4), dk + ((4 * kChunk + kr * 32) >> 4), idesc_qk, 1u);
+        mma_commit_warp(BAR(B_S_FULL + sb));
+        if (j > pc.y) {
+          const uint32_t tp = t - 1;
+          if (!warp_ok(mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag,
+                                 kWaitNs))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t dk = dKt + ((sb * kKTile) >> 4);
-          const uint32_t d = tbase + kColS + 64 * sb;
-#pragma unroll
-          for (uint32_t kc = 0; kc < 16; ++kc)
-            mma_ts(d, tbase + kColQ + 8 * kc, dk + (((kc >> 2) * kChunk + (kc & 3) * 32) >> 4),
-                   idesc_qk, kc > 0 ? 1u : 0u);
-#pragma unroll
-          for (uint32_t kr = 0; kr < 2; ++kr)
-            mma_ss(d, dQr + ((kr * 32) >> 4), dk + ((4 * kChunk + kr * 32) >> 4), idesc_qk, 1u);
-          mma_commit(BAR(B_S_FULL + sb));
-          if (j > pc.y) {
-            const uint32_t tp = t - 1;
-            if (!mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag, kWaitNs)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv(tp, j - 1 == pc.y);
-          }
+          issue_pv(tp, j - 1 == pc.y);
         }
-        if (!ok) break;
-        const uint32_t tp = t - 1;
-        if (!mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag, kWaitNs)) break;
-        tc_fence_after();
-        issue_pv(tp, pc.z - 1 == pc.y);
       }
-      // no MMA may be in flight when tensor memory is released
-      mma_commit(BAR(B_DRAIN));
-      wait_noabort(BAR(B_DRAIN), 0);
+      if (!ok) break;
+      const uint32_t tp = t - 1;
+      if (!warp_ok(mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag, kWaitNs)))
+        break;
+      tc_fence_after();
+      issue_pv(tp, pc.z - 1 == pc.y);
     }
+    // no MMA may be in flight when tensor memory is released
+    mma_commit_warp(BAR(B_DRAIN));
+    if (lane == 0) wait_noabort(BAR(B_DRAIN), 0);
+    __syncwarp();
   } else if (warp >= kSoftmaxWarp0 && warp < kDequantWarp0) {
     // ------------------------------------------------------------ softmax
     const uint32_t quad = uint32_t(warp & 3);
