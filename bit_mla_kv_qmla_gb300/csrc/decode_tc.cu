@@ -21,10 +21,16 @@
 // Tensor memory per CTA: O_r cols 0-255, Qc_r cols 256-383, S/P double
 // buffer cols 384-511.
 //
-// Warp roles (14 warps): 0 bulk-copy producer, 1 MMA issuer (one thread),
-// 2-5 softmax (thread = head), 6-13 dequantization.  Dequantized operands
-// are binary16 (code*scale + zero, exact by construction of the quantizer's
-// grid); queries are converted bf16 -> binary16; accumulation is binary32.
+// Warp roles (14 warps): 0 bulk-copy producer, 1 MMA issuer, 2-5 softmax
+// (thread = head), 6-13 dequantization.  Dequantized operands are binary16
+// (code*scale + zero, exact by construction of the quantizer's grid);
+// queries are converted bf16 -> binary16; accumulation is binary32.
+//
+// The same kernel serves the uncompressed BF16 cache, the baseline the
+// low-bit formats are compared with: operands stay bfloat16 (queries, cache
+// and P), nothing is dequantized, and the "dequantization" warps load each
+// tile's rows straight from HBM (256-bit loads, one tile ahead) into the
+// swizzled operand tile; the producer warp has nothing to do.
 // The softmax is online in base 2 with lazy rescaling: O and l are rescaled
 // only when a tile's maximum exceeds the running one by more than 8
 // (P <= 256).  Every wait is bounded in time; on timeout the CTA raises an
@@ -122,7 +128,15 @@ enum : uint32_t {
   B_P_FULL = 14, B_PV_DONE = 16, B_X_FULL = 18, B_X_EMPTY = 20, B_Q_FULL = 22, B_DRAIN = 23
 };
 
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
 // ---------------------------------------------------------------- kernel
+template <bool kBF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc128_kernel(DecodeArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -135,6 +149,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
   const Geom G = geom(a.fmt);
+  // binary16 or bfloat16 operands
+  auto pack2 = [](float lo, float hi) { return kBF16 ? pack_bf162(lo, hi) : pack_half2(lo, hi); };
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < kStages; ++i) {
@@ -169,7 +185,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kSmTslot);
   const int2 wr = a.ws.wrange[pair];
 
-  if (warp == 0) {
+  if (warp == 0 && !kBF16) {
     // ------------------------------------------------------------ producer
     uint32_t t = 0;
     bool ok = true;
@@ -214,8 +230,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop converged and an elected lane issues each
     // instruction (single-lane issue behind waits and branches costs several
     // times more per MMA).
-    const uint32_t idesc_qk = idesc_f16(128, 64, false, false);
-    const uint32_t idesc_pv = idesc_f16(128, 256, false, true);
+    const uint32_t idesc_qk = kBF16 ? idesc_bf16(128, 64, false, false)
+                                    : idesc_f16(128, 64, false, false);
+    const uint32_t idesc_pv = kBF16 ? idesc_bf16(128, 256, false, true)
+                                    : idesc_f16(128, 256, false, true);
     // operand descriptors; an offset advances the 16-byte address field
     const uint64_t dKt = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
     const uint64_t dCt = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
@@ -309,8 +327,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              w[4 * i + k] = pack_half2(__uint_as_float(in[k] << 16),
-                                        __uint_as_float(in[k] & 0xffff0000u));
+              w[4 * i + k] = kBF16 ? in[k]
+                                   : pack_half2(__uint_as_float(in[k] << 16),
+                                                __uint_as_float(in[k] & 0xffff0000u));
           }
           tmem_st32(tbase + lane_base + kColQ + c0 / 2, w);
         }
@@ -323,7 +342,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t o[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xffff0000u));
+            o[k] = kBF16 ? in[k]
+                         : pack_half2(__uint_as_float(in[k] << 16),
+                                      __uint_as_float(in[k] & 0xffff0000u));
           *reinterpret_cast<uint4*>(qr + ((g ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();
@@ -433,7 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float p0 = ex2_approx(sv[2 * i] - msub);
           const float p1 = ex2_approx(sv[2 * i + 1] - msub);
           ls4[i & 3] += p0 + p1;
-          pk[i] = pack_half2(p0, p1);
+          pk[i] = pack2(p0, p1);
         }
         const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         l_run += ls;
@@ -465,6 +486,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         a.ws.part_lse[int64_t(s) * 128 + h] =
             l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       tc_fence_before();
+    }
+  } else if (warp >= kDequantWarp0 && kBF16) {
+    // ------------------------------------------------------------ BF16 rows
+    // thread dt owns token tt and 16-channel segment seg of each of the 4
+    // groups of this half (and, dt < 128, a 16-channel RoPE segment); the
+    // rows of the next tile are in flight while this tile's are stored
+    const int dt = int(threadIdx.x) - kDequantWarp0 * 32;
+    const int tt = (dt >> 2) & 63, seg = dt & 3;
+    const int rtt = dt >> 1, rseg = dt & 1;  // RoPE (dt < 128)
+    uint32_t t = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      if (pc.z <= pc.y) continue;
+      const int L = seq_len_clamped(a, pc.x);
+      const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
+      // rows of block j of this CTA's half, or nullptr (past the piece or a
+      // bad block id: zeros); n = valid token rows
+      auto half_of = [&](int j, int& n) -> const uint8_t* {
+        n = 0;
+        if (j >= pc.z) return nullptr;
+        const int32_t blk = btab[j];
+        if (blk < 0 || blk >= a.num_blocks) {
+          if (dt == 0) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
+          return nullptr;
+        }
+        n = min(kT, L - j * kT);
+        return a.blocks + int64_t(blk) * G.block + rank * G.half;
+      };
+      auto load_rows = [&](const uint8_t* hb, int n, uint32_t (&c)[4][8], uint32_t (&r)[8]) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          if (hb && tt < n) {
+            ld_nc_v8(hb + (g * 64 + tt) * 128 + seg * 32, c[g]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) c[g][e] = 0u;
+          }
+        }
+        if (dt < 128 && hb && rtt < n) {
+          ld_nc_v8(hb + G.rope_off + rtt * 64 + rseg * 32, r);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) r[e] = 0u;
+        }
+      };
+      int n_cur;
+      const uint8_t* hb_cur = half_of(pc.y, n_cur);
+      uint32_t cn[4][8], rn[8];
+      load_rows(hb_cur, n_cur, cn, rn);
+      for (int j = pc.y; j < pc.z; ++j, ++t) {
+        uint32_t cc[4][8], rc[8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cc[g][e] = cn[g][e];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rc[e] = rn[e];
+        int n_next;
+        const uint8_t* hb_next = half_of(j + 1, n_next);
+        load_rows(hb_next, n_next, cn, rn);
+        const uint32_t kb = t & 1u;
+        if (!warp_ok(mbar_wait(BAR(B_K_EMPTY + kb), ((t >> 1) & 1u) ^ 1u, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        unsigned char* kt = sm + kSmK + kb * kKTile;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) st_row16(kt + g * kChunk, tt, seg, cc[g]);
+        if (dt < 128) st_row16(kt + 4 * kChunk, rtt, rseg, rc);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_K_FULL + kb));
+      }
     }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant
@@ -547,12 +642,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_decode_tc128(const DecodeArgs& a, cudaStream_t stream) {
-  static int smem_attr_done[kMaxDevices];
+  static int smem_attr_done[kMaxDevices], smem_attr_done_bf16[kMaxDevices];
   cudaError_t e = launch_plan(a, stream);
   if (e != cudaSuccess) return e;
-  e = ensure_smem_attr(decode_tc128_kernel, int(kSmDyn), smem_attr_done);
+  const bool bf16 = a.fmt == QMLA_BF16;
+  auto kernel = bf16 ? decode_tc128_kernel<true> : decode_tc128_kernel<false>;
+  e = ensure_smem_attr(kernel, int(kSmDyn), bf16 ? smem_attr_done_bf16 : smem_attr_done);
   if (e != cudaSuccess) return e;
-  decode_tc128_kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(a);
+  kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -562,7 +659,8 @@ int tc_workers(int sms, int heads) {
 }
 
 bool tc_supported(int fmt, int heads) {
-  return (heads == 128 || heads == 16) && (fmt == QMLA_C4R4 || fmt == QMLA_C2R4);
+  if (heads == 128) return fmt == QMLA_C4R4 || fmt == QMLA_C2R4 || fmt == QMLA_BF16;
+  return heads == 16 && (fmt == QMLA_C4R4 || fmt == QMLA_C2R4);
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
