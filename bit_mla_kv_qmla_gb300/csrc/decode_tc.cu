@@ -27,9 +27,11 @@
 // queries are converted bf16 -> binary16; accumulation is binary32.
 //
 // The same kernel serves the uncompressed BF16 cache, the baseline the
-// low-bit formats are compared with: operands stay bfloat16 (queries, cache
-// and P), nothing is dequantized, and the "dequantization" warps load each
-// tile's rows straight from HBM (256-bit loads, one tile ahead) into the
+// low-bit formats are compared with: nothing is dequantized; the
+// "dequantization" warps load each tile's rows straight from HBM (256-bit
+// loads, one tile ahead), convert them bfloat16 -> binary16 (exact for cache
+// values in binary16's normal range; P, the other operand of P.V, needs
+// binary16's 11 significant bits at long contexts) and store them into the
 // swizzled operand tile; the producer warp has nothing to do.
 // The softmax is online in base 2 with lazy rescaling: O and l are rescaled
 // only when a tile's maximum exceeds the running one by more than 8
@@ -149,8 +151,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
   const Geom G = geom(a.fmt);
-  // binary16 or bfloat16 operands
-  auto pack2 = [](float lo, float hi) { return kBF16 ? pack_bf162(lo, hi) : pack_half2(lo, hi); };
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < kStages; ++i) {
@@ -230,10 +230,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop converged and an elected lane issues each
     // instruction (single-lane issue behind waits and branches costs several
     // times more per MMA).
-    const uint32_t idesc_qk = kBF16 ? idesc_bf16(128, 64, false, false)
-                                    : idesc_f16(128, 64, false, false);
-    const uint32_t idesc_pv = kBF16 ? idesc_bf16(128, 256, false, true)
-                                    : idesc_f16(128, 256, false, true);
+    const uint32_t idesc_qk = idesc_f16(128, 64, false, false);
+    const uint32_t idesc_pv = idesc_f16(128, 256, false, true);
     // operand descriptors; an offset advances the 16-byte address field
     const uint64_t dKt = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
     const uint64_t dCt = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
@@ -327,9 +325,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              w[4 * i + k] = kBF16 ? in[k]
-                                   : pack_half2(__uint_as_float(in[k] << 16),
-                                                __uint_as_float(in[k] & 0xffff0000u));
+              w[4 * i + k] = pack_half2(__uint_as_float(in[k] << 16),
+                                        __uint_as_float(in[k] & 0xffff0000u));
           }
           tmem_st32(tbase + lane_base + kColQ + c0 / 2, w);
         }
@@ -342,9 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t o[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            o[k] = kBF16 ? in[k]
-                         : pack_half2(__uint_as_float(in[k] << 16),
-                                      __uint_as_float(in[k] & 0xffff0000u));
+            o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xffff0000u));
           *reinterpret_cast<uint4*>(qr + ((g ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();
@@ -454,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float p0 = ex2_approx(sv[2 * i] - msub);
           const float p1 = ex2_approx(sv[2 * i + 1] - msub);
           ls4[i & 3] += p0 + p1;
-          pk[i] = pack2(p0, p1);
+          pk[i] = pack_half2(p0, p1);
         }
         const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         l_run += ls;
@@ -553,9 +548,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         unsigned char* kt = sm + kSmK + kb * kKTile;
+        auto to_f16 = [](uint32_t (&w)[8]) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) st_row16(kt + g * kChunk, tt, seg, cc[g]);
-        if (dt < 128) st_row16(kt + 4 * kChunk, rtt, rseg, rc);
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+        };
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          to_f16(cc[g]);
+          st_row16(kt + g * kChunk, tt, seg, cc[g]);
+        }
+        if (dt < 128) {
+          to_f16(rc);
+          st_row16(kt + 4 * kChunk, rtt, rseg, rc);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_K_FULL + kb));
@@ -659,8 +665,8 @@ int tc_workers(int sms, int heads) {
 }
 
 bool tc_supported(int fmt, int heads) {
-  if (heads == 128) return fmt == QMLA_C4R4 || fmt == QMLA_C2R4 || fmt == QMLA_BF16;
-  return heads == 16 && (fmt == QMLA_C4R4 || fmt == QMLA_C2R4);
+  return (heads == 128 || heads == 16) &&
+         (fmt == QMLA_C4R4 || fmt == QMLA_C2R4 || fmt == QMLA_BF16);
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {

@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmAbort);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int worker = blockIdx.x;
-  const Geom G = geom(kCBits == 4 ? QMLA_C4R4 : QMLA_C2R4);
+  constexpr bool kBF16 = kCBits == 16;  // uncompressed cache (rows converted to binary16)
+  const Geom G = geom(kCBits == 4 ? QMLA_C4R4 : kCBits == 2 ? QMLA_C2R4 : QMLA_BF16);
 
   if (threadIdx.x == 0) {
     for (uint32_t h = 0; h < 2; ++h) {
@@ -493,6 +494,111 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
       tc_fence_before();
       named_bar_sync(1, 128);  // red_sum is read by all before the next piece reuses it
     }
+  } else if (warp >= kDequantWarp0 && kBF16) {
+    // ------------------------------------------------------------ BF16 rows
+    // The same split as the dequantization below (lane quarter q, column
+    // half dw; content groups 4h+2dw, 4h+2dw+1 and RoPE channels
+    // 32h+16dw .. +15 of half h), but the rows only change type: each item
+    // (a 64-channel group row of 128 B, or 16 RoPE channels) is loaded one
+    // item ahead, converted bfloat16 -> binary16 (exact for cache values in
+    // binary16's normal range) and stored to tensor memory and shared memory.
+    // Binary16 rather than bfloat16 operands because P is the other operand
+    // of P.V: P in bfloat16 (8 significant bits) misses the 1e-2 output
+    // tolerance at long contexts, P in binary16 (11) does not.
+    const int q = warp & 3, dw = (warp - kDequantWarp0) >> 2;
+    const int r = 32 * q + lane, bi = q >> 1, tt = r & 63;
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    const uint32_t vrow_off = uint32_t((r >> 3) * 1024 + (r & 7) * 128);
+    const int sw7 = r & 7;
+    uint32_t t = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      if (pc.z <= pc.y) continue;
+      const int L = seq_len_clamped(a, pc.x);
+      const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
+      // rows of this thread's token in the tile starting at jt (nullptr: none
+      // or a bad block id, read as zeros)
+      auto tile_rows = [&](int jt) -> const uint8_t* {
+        const int j = jt + bi;
+        if (j >= pc.z) return nullptr;
+        const int32_t blk = btab[j];
+        if (blk < 0 || blk >= a.num_blocks) {
+          if (lane == 0) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
+          return nullptr;
+        }
+        return (tt < min(kT, L - j * kT)) ? a.blocks + int64_t(blk) * G.block : nullptr;
+      };
+      // item k of half h: 0, 1 content groups 2dw+k; 2 the RoPE segment
+      auto load_item = [&](const uint8_t* blk, int h, int k, uint32_t (&w)[32]) {
+        if (blk == nullptr) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = 0u;
+          return;
+        }
+        const uint8_t* half = blk + h * G.half;
+        if (k < 2) {
+          const uint8_t* row = half + ((2 * dw + k) * 64 + tt) * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ld_nc_v8(row + 32 * i, w + 8 * i);
+        } else {
+          ld_nc_v8(half + G.rope_off + tt * 64 + dw * 32, w);
+        }
+      };
+      const uint8_t* rows_cur = tile_rows(pc.y);
+      uint32_t nxt[32];
+      load_item(rows_cur, 0, 0, nxt);
+      for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
+        const uint8_t* rows_next = tile_rows(jt + 2);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t hn = 2 * t + uint32_t(h), grp = hn % 3;
+          bool got = mbar_wait(BAR(B_K_EMPTY + h), (t & 1u) ^ 1u, abort_flag, kWaitNs);
+          got = got && mbar_wait(BAR(B_V_EMPTY + grp), ((hn / 3) & 1u) ^ 1u, abort_flag, kWaitNs);
+          if (!warp_ok(got)) {
+            ok = false;
+            break;
+          }
+          unsigned char* vgrp = sm + kSmV + grp * kGroup + vrow_off;
+#pragma unroll 1
+          for (int k = 0; k < 3; ++k) {
+            uint32_t cur[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              cur[e] = pack_half2(__uint_as_float(nxt[e] << 16),
+                                  __uint_as_float(nxt[e] & 0xffff0000u));
+            // the next item: this half's next one, else the next half's first
+            if (k < 2)
+              load_item(rows_cur, h, k + 1, nxt);
+            else if (h == 0)
+              load_item(rows_cur, 1, 0, nxt);
+            else
+              load_item(rows_next, 0, 0, nxt);
+            if (k < 2) {
+              const int c = 4 * h + 2 * dw + k;
+              tmem_st32(tbase + lane_base + kColK + 32 * c, cur);
+              unsigned char* row = vgrp + (c & 3) * kChunk;
+#pragma unroll
+              for (int g = 0; g < 8; ++g)
+                *reinterpret_cast<uint4*>(row + ((g ^ sw7) << 4)) =
+                    make_uint4(cur[4 * g], cur[4 * g + 1], cur[4 * g + 2], cur[4 * g + 3]);
+            } else {
+              uint32_t v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = cur[e];
+              tmem_st8(tbase + lane_base + kColRope + 16 * h + 8 * dw, v);
+            }
+          }
+          tmem_wait_st();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_K_FULL + h));
+        }
+        if (!ok) break;
+        rows_cur = rows_next;
+      }
+    }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant
     // warp: lane quarter q (tensor-memory lanes 32q..32q+31 = token rows) and
@@ -612,11 +718,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
 }  // namespace
 
 cudaError_t launch_decode_tc16(const DecodeArgs& a, cudaStream_t stream) {
-  static int smem_attr_done[kMaxDevices], smem_attr_done2[kMaxDevices];
+  static int smem_attr_done[kMaxDevices], smem_attr_done2[kMaxDevices],
+      smem_attr_done_bf16[kMaxDevices];
   cudaError_t e = launch_plan(a, stream);
   if (e != cudaSuccess) return e;
-  auto kernel = (a.fmt == QMLA_C4R4) ? decode_tc16_kernel<4> : decode_tc16_kernel<2>;
-  e = ensure_smem_attr(kernel, int(kSmDyn), a.fmt == QMLA_C4R4 ? smem_attr_done : smem_attr_done2);
+  auto kernel = (a.fmt == QMLA_C4R4)   ? decode_tc16_kernel<4>
+                : (a.fmt == QMLA_C2R4) ? decode_tc16_kernel<2>
+                                       : decode_tc16_kernel<16>;
+  e = ensure_smem_attr(kernel, int(kSmDyn),
+                       a.fmt == QMLA_C4R4   ? smem_attr_done
+                       : a.fmt == QMLA_C2R4 ? smem_attr_done2
+                                            : smem_attr_done_bf16);
   if (e != cudaSuccess) return e;
   kernel<<<dim3(unsigned(a.workers)), kThreads, kSmDyn, stream>>>(a);
   return cudaGetLastError();

@@ -177,7 +177,9 @@ size_t qmla_decode_workspace_bytes(int format, int32_t batch, int32_t heads,
  *   workspace         device scratch of >= qmla_decode_workspace_bytes(...)
  *                     bytes, 256-byte aligned; contents need no initialization
  * The tensor-core kernels take queries as binary16 operands: |q| must stay
- * below 65504.  Errors: INVALID_ARG, UNSUPPORTED (format, heads), WORKSPACE,
+ * below 65504; with the BF16 cache they convert cache values to binary16 as
+ * well, so those must stay below 65504 too (values under 2^-14 keep only
+ * binary16's subnormal precision).  Errors: INVALID_ARG, UNSUPPORTED (format, heads), WORKSPACE,
  * CUDA.  Sequences longer than max_seq_len or their block table set
  * QMLA_STATUS_BAD_LEN and are truncated. */
 int qmla_decode(int format, const void* blocks, int64_t num_blocks,
