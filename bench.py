@@ -317,7 +317,7 @@ def measure_also(args, device):
     from bit_mla_kv_qmla_gb300.cache import Decoder, build_cache
     out = {}
     pk = peaks()
-    for cfg, fmt in [(4, "C4R4"), (4, "C2R4"), (4, "BF16"), (2, "C4R4"), (3, "C2R4")]:
+    for cfg, fmt in [(1, "BF16"), (4, "C4R4"), (4, "C2R4"), (4, "BF16"), (2, "C4R4"), (3, "C2R4")]:
         w = W.with_format(W.WORKLOADS[cfg], fmt)
         lens = W.seq_lens(w)
         cache = build_cache(w, device)
