@@ -12,14 +12,16 @@
 // 32r..32r+31, which is exactly one contiguous half of every cache block.
 //   QK : S_r[128 heads x 64 tok] = Qc_r (A, tensor memory) x K_r^T (B, smem)
 //                                + Qr_r (A, smem)          x R_r^T (B, smem)
-//        the two partial scores are exchanged through cluster shared memory
-//        with asynchronous remote stores that complete on the receiver's
-//        mbarrier, and added (binary32 addition commutes, so both CTAs hold
-//        the same S, the same softmax and the same P);
-//   PV : O_r[128 x 256] += P (A, tensor memory, aliasing S) x C_r (B, the same
-//        dequantized smem tile read MN-major).
-// Tensor memory per CTA: O_r cols 0-255, Qc_r cols 256-383, S/P double
-// buffer cols 384-511.
+//        the softmax of heads 64r..64r+63 runs on CTA r: each CTA sends the
+//        partial scores of the other CTA's heads (16 KB per tile) through
+//        cluster shared memory with asynchronous remote stores that complete
+//        on the receiver's mbarrier, adds the partials it receives for its
+//        own heads, and sends back those heads' P rows (binary16, 8 KB) with
+//        their rescale factors, so both CTAs end up with the full P tile;
+//   PV : O_r[128 x 256] += P (A, smem) x C_r (B, the same dequantized smem
+//        tile read MN-major).
+// Tensor memory per CTA: O_r cols 0-255, Qc_r cols 256-383, S double buffer
+// cols 384-511.
 //
 // Warp roles (14 warps): 0 bulk-copy producer, 1 MMA issuer, 2-5 softmax
 // (thread = head), 6-13 dequantization.  Dequantized operands are binary16
@@ -115,10 +117,15 @@ constexpr uint32_t kKTile = 5 * kChunk;              // 4 content chunks + RoPE 
 constexpr uint32_t kStages = 4;                      // bulk-copy ring depth
 constexpr uint32_t kSmStage = kSmK + 2 * kKTile;     // kStages x staging
 constexpr uint32_t kStage = 10240 + 256;             // largest half + RoPE scale/zero
-constexpr uint32_t kSmX = kSmStage + kStages * kStage;  // 2 x score exchange
-constexpr uint32_t kX = 128 * 64 * 4;
-constexpr uint32_t kSmBar = kSmX + 2 * kX;
-constexpr uint32_t kNumBars = 24;
+constexpr uint32_t kSmX = kSmStage + kStages * kStage;  // 2 x received partial scores
+constexpr uint32_t kX = 64 * 64 * 4;                 // [64 own heads][64 tok] fp32
+constexpr uint32_t kSmPt = kSmX + 2 * kX;            // 2 x P tile
+constexpr uint32_t kPt = 128 * 128;                  // [128 heads][64 tok] fp16 SW128
+constexpr uint32_t kSmAlpha = kSmPt + 2 * kPt;       // 2 x [64] received rescale factors
+constexpr uint32_t kSmLx = kSmAlpha + 2 * 256;       // [64] received row sums (per piece)
+constexpr uint32_t kPx = 64 * 128 + 64 * 4;          // P rows + rescale factors per tile
+constexpr uint32_t kSmBar = kSmLx + 256;
+constexpr uint32_t kNumBars = 27;
 constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
 constexpr uint32_t kSmBytes = kSmAbort + 60;
@@ -127,8 +134,10 @@ constexpr uint32_t kSmDyn = kSmBytes + 1024;         // slack for 1 KB alignment
 // barrier indices
 enum : uint32_t {
   B_STAGE_FULL = 0, B_STAGE_EMPTY = 4, B_K_FULL = 8, B_K_EMPTY = 10, B_S_FULL = 12,
-  B_P_FULL = 14, B_PV_DONE = 16, B_X_FULL = 18, B_X_EMPTY = 20, B_Q_FULL = 22, B_DRAIN = 23
+  B_P_FULL = 14, B_PV_DONE = 16, B_X_FULL = 18, B_X_EMPTY = 20, B_Q_FULL = 22, B_DRAIN = 23,
+  B_PX_FULL = 24, B_LX_FULL = 26
 };
+static_assert(kSmPt % 1024 == 0, "SW128 operand tiles are 1 KB aligned");
 
 __device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* r) {
   asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -164,13 +173,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(BAR(B_P_FULL + i), 128);
       mbar_init(BAR(B_PV_DONE + i), 1);
       mbar_init(BAR(B_X_FULL + i), 1);
-      mbar_init(BAR(B_X_EMPTY + i), 128);
+      mbar_init(BAR(B_X_EMPTY + i), 64);  // the peer's 64 owning threads
+      mbar_init(BAR(B_PX_FULL + i), 1);
     }
     mbar_init(BAR(B_Q_FULL), 128);
     mbar_init(BAR(B_DRAIN), 1);
-    // the first two score exchanges are expected before the peer can send them
+    mbar_init(BAR(B_LX_FULL), 1);
+    // the first exchanges are expected before the peer can send them
     mbar_arrive_expect_tx(BAR(B_X_FULL + 0), kX);
     mbar_arrive_expect_tx(BAR(B_X_FULL + 1), kX);
+    mbar_arrive_expect_tx(BAR(B_PX_FULL + 0), kPx);
+    mbar_arrive_expect_tx(BAR(B_PX_FULL + 1), kPx);
+    mbar_arrive_expect_tx(BAR(B_LX_FULL), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -236,13 +250,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint64_t dKt = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
     const uint64_t dCt = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
     const uint64_t dQr = smem_desc(sb0 + kSmQr, 16, 1024, kSwizzle128B);
+    const uint64_t dPt = smem_desc(sb0 + kSmPt, 16, 1024, kSwizzle128B);
     uint32_t t = 0, piece = 0;
     bool ok = true;
     auto issue_pv = [&](uint32_t tt, bool first) {
       const uint32_t sb = tt & 1u;
 #pragma unroll
       for (uint32_t kk = 0; kk < 4; ++kk) {
-        mma_ts_warp(tbase + kColO, tbase + kColS + 64 * sb + 8 * kk,
+        mma_ss_warp(tbase + kColO, dPt + ((sb * kPt + kk * 32) >> 4),
                     dCt + ((sb * kKTile + kk * 2048) >> 4), idesc_pv,
                     (first && kk == 0) ? 0u : 1u);
       }
@@ -298,18 +313,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kSoftmaxWarp0 && warp < kDequantWarp0) {
     // ------------------------------------------------------------ softmax
+    // thread = head h (tensor-memory lane).  CTA r owns heads 64r..64r+63
+    // (lane quarters 2r, 2r+1): their softmax runs here.  The other two warps
+    // send the peer the partial scores of the peer's heads and then take the
+    // peer's P rows and rescale factors for them.
     const uint32_t quad = uint32_t(warp & 3);
     const int h = int(quad * 32) + lane;
+    const bool own = (quad >> 1) == rank;
+    const int hx = h & 63;  // row of h in the exchange buffers of its owner
     const uint32_t lane_base = (quad * 32u) << 16;
     const float c2 = a.scale * 1.4426950408889634f;  // scores to log2 units
-    uint32_t t = 0;
+    // row h of a P tile (SW128 K-major, 64 tokens = 128 B)
+    const uint32_t prow = kSmPt + uint32_t(h >> 3) * 1024u + uint32_t(h & 7) * 128u;
+    uint32_t t = 0, piece = 0;
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
       const int4 pc = a.ws.pieces[s];
       const int b = pc.x;
       if (pc.z <= pc.y) {  // no block: an empty partial (the planner produces none)
         for (int c = 0; c < 256; ++c) a.ws.part_o[(int64_t(s) * 128 + h) * kDc + 256 * rank + c] = 0.f;
-        if (rank == 0) a.ws.part_lse[int64_t(s) * 128 + h] = -INFINITY;
+        if (own) a.ws.part_lse[int64_t(s) * 128 + h] = -INFINITY;
         continue;
       }
       const int L = seq_len_clamped(a, b);
@@ -347,7 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(BAR(B_Q_FULL));
       }
-      float m_run = -INFINITY, l_run = 0.0f;
+      float m_run = -INFINITY, l_run = 0.0f;  // own heads
       uint32_t vmask = 0;
       for (int j = pc.y; j < pc.z; ++j, ++t) {
         if (((j - pc.y) & 31) == 0) vmask = valid_mask(a, b, j, pc.z);
@@ -369,92 +392,121 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             sv[32 + i] = __uint_as_float(r1[i]);
           }
         }
-        // exchange partial scores with the peer CTA
-        if (!warp_ok(mbar_wait<true>(BAR(B_X_EMPTY + sb), par ^ 1u, abort_flag, kWaitNs))) {
-          ok = false;
-          break;
-        }
-        const uint32_t xrow = kSmX + sb * kX + uint32_t(h) * 256u;
-        {
-          const uint32_t prow = mapa(sb0 + xrow, peer);
-          const uint32_t pbar = mapa(BAR(B_X_FULL + sb), peer);
+        float alpha = 1.0f;
+        if (!own) {
+          // --- the peer's head: send its partial scores, take back P and the
+          // rescale factor.  (The peer writes P into this CTA's tile only after
+          // these scores arrive, and they leave only after this CTA's QK of
+          // tile t, i.e. after its P.V of tile t-2 read that tile parity.)
+          if (!warp_ok(mbar_wait<true>(BAR(B_X_EMPTY + sb), par ^ 1u, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          {
+            const uint32_t xrow = mapa(sb0 + kSmX + sb * kX + uint32_t(hx) * 256u, peer);
+            const uint32_t pbar = mapa(BAR(B_X_FULL + sb), peer);
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            st_async_v4(prow + ((uint32_t(q) ^ uint32_t(h & 15)) << 4), sv[4 * q],
-                        sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3], pbar);
-        }
-        if (!warp_ok(mbar_wait<true>(BAR(B_X_FULL + sb), par, abort_flag, kWaitNs))) {
-          ok = false;
-          break;
-        }
+            for (int q = 0; q < 16; ++q)
+              st_async_v4(xrow + ((uint32_t(q) ^ uint32_t(hx & 15)) << 4), sv[4 * q],
+                          sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3], pbar);
+          }
+          if (!warp_ok(mbar_wait<true>(BAR(B_PX_FULL + sb), par, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          alpha = *reinterpret_cast<const volatile float*>(sm + kSmAlpha + sb * 256 + hx * 4);
+          // expect this buffer's next exchange (tile t+2) before the peer can
+          // send it: the peer sends it only after scores this thread sends
+          // later have arrived
+          if (hx == 0) mbar_arrive_expect_tx(BAR(B_PX_FULL + sb), kPx);
+        } else {
+          // --- this CTA's head: add the peer's partial, softmax, send P back
+          if (!warp_ok(mbar_wait<true>(BAR(B_X_FULL + sb), par, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          const uint32_t xrow = kSmX + sb * kX + uint32_t(hx) * 256u;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(sm + xrow + ((q ^ (h & 15)) << 4));
-          sv[4 * q] += v.x;
-          sv[4 * q + 1] += v.y;
-          sv[4 * q + 2] += v.z;
-          sv[4 * q + 3] += v.w;
-        }
-        // this CTA's buffer sb is read: expect the exchange two tiles ahead and
-        // tell the peer it may send it
-        if (h == 0) mbar_arrive_expect_tx(BAR(B_X_FULL + sb), kX);
-        mbar_arrive_remote(mapa(BAR(B_X_EMPTY + sb), peer));
+          for (int q = 0; q < 16; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(sm + xrow + ((q ^ (hx & 15)) << 4));
+            sv[4 * q] += v.x;
+            sv[4 * q + 1] += v.y;
+            sv[4 * q + 2] += v.z;
+            sv[4 * q + 3] += v.w;
+          }
+          // this CTA's buffer sb is read: expect the exchange two tiles ahead
+          // and tell the peer it may send it
+          if (hx == 0) mbar_arrive_expect_tx(BAR(B_X_FULL + sb), kX);
+          mbar_arrive_remote(mapa(BAR(B_X_EMPTY + sb), peer));
 
-        const int nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
+          const int nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sv[i] *= c2;
-        if (nvalid < 64) {
+          for (int i = 0; i < 64; ++i) sv[i] *= c2;
+          if (nvalid < 64) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) sv[i] = (i < nvalid) ? sv[i] : -INFINITY;
-        }
-        float mx8[8];
+            for (int i = 0; i < 64; ++i) sv[i] = (i < nvalid) ? sv[i] : -INFINITY;
+          }
+          float mx8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          mx8[k] = fmaxf(fmaxf(fmaxf(sv[8 * k], sv[8 * k + 1]), fmaxf(sv[8 * k + 2], sv[8 * k + 3])),
-                         fmaxf(fmaxf(sv[8 * k + 4], sv[8 * k + 5]), fmaxf(sv[8 * k + 6], sv[8 * k + 7])));
-        }
-        const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        const bool need = mt > m_run + 8.0f;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? mt : m_run;
-          const float alpha = need ? exp2f(m_run - m_new) : 1.0f;
-          if (j > pc.y) {
-            const uint32_t tp = t - 1;
-            if (!warp_ok(mbar_wait(BAR(B_PV_DONE + (tp & 1u)), (tp >> 1) & 1u, abort_flag,
-                                   kWaitNs))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll 1
-            for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
-              uint32_t o[32];
-              tmem_ld32(tbase + lane_base + kColO + c0, o);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tbase + lane_base + kColO + c0, o);
-            }
-            tmem_wait_st();
+          for (int k = 0; k < 8; ++k) {
+            mx8[k] = fmaxf(fmaxf(fmaxf(sv[8 * k], sv[8 * k + 1]), fmaxf(sv[8 * k + 2], sv[8 * k + 3])),
+                           fmaxf(fmaxf(sv[8 * k + 4], sv[8 * k + 5]), fmaxf(sv[8 * k + 6], sv[8 * k + 7])));
+          }
+          const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          if (mt > m_run + 8.0f) {
+            alpha = exp2f(m_run - mt);
+            m_run = mt;
           }
           l_run *= alpha;
-          m_run = m_new;
-        }
-        uint32_t pk[32];
-        float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        const float msub = (mt == -INFINITY) ? 0.0f : m_run;  // all masked: every p is 0
+          uint32_t pk[32];
+          float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          const float msub = (mt == -INFINITY) ? 0.0f : m_run;  // all masked: every p is 0
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(sv[2 * i] - msub);
-          const float p1 = ex2_approx(sv[2 * i + 1] - msub);
-          ls4[i & 3] += p0 + p1;
-          pk[i] = pack_half2(p0, p1);
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2_approx(sv[2 * i] - msub);
+            const float p1 = ex2_approx(sv[2 * i + 1] - msub);
+            ls4[i & 3] += p0 + p1;
+            pk[i] = pack_half2(p0, p1);
+          }
+          l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+          // P row h into this CTA's tile and the peer's, the factor to the peer
+          const uint32_t pl = prow + sb * kPt;
+          const uint32_t pr = mapa(sb0 + pl, peer);
+          const uint32_t pbar = mapa(BAR(B_PX_FULL + sb), peer);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t off = uint32_t((g ^ (h & 7)) << 4);
+            *reinterpret_cast<uint4*>(sm + pl + off) =
+                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            st_async_u32x4(pr + off, pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3], pbar);
+          }
+          st_async_f32(mapa(sb0 + kSmAlpha + sb * 256 + hx * 4, peer), alpha, pbar);
         }
-        const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-        l_run += ls;
-        tmem_st32(tbase + lane_base + kColS + 64 * sb, pk);
-        tmem_wait_st();
+        // rescale this CTA's O rows of head h (its 256 channels) when the
+        // maximum moved; the P.V products of tile t-1 must have landed first
+        if (__any_sync(0xffffffffu, alpha != 1.0f) && j > pc.y) {
+          const uint32_t tp = t - 1;
+          if (!warp_ok(mbar_wait(BAR(B_PV_DONE + (tp & 1u)), (tp >> 1) & 1u, abort_flag,
+                                 kWaitNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tbase + lane_base + kColO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tbase + lane_base + kColO + c0, o);
+          }
+          tmem_wait_st();
+        }
+        // this tile's P rows (written here or by the peer) reach the tensor
+        // cores through the async proxy
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(BAR(B_P_FULL + sb));
       }
@@ -464,7 +516,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!warp_ok(mbar_wait(BAR(B_PV_DONE + (tl & 1u)), (tl >> 1) & 1u, abort_flag, kWaitNs)))
         break;
       tc_fence_after();
-      const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      float l = l_run;
+      if (own) {
+        st_async_f32(mapa(sb0 + kSmLx + hx * 4, peer), l_run, mapa(BAR(B_LX_FULL), peer));
+        a.ws.part_lse[int64_t(s) * 128 + h] =
+            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      } else {
+        if (!warp_ok(mbar_wait<true>(BAR(B_LX_FULL), piece & 1u, abort_flag, kWaitNs))) break;
+        l = *reinterpret_cast<const volatile float*>(sm + kSmLx + hx * 4);
+        __syncwarp();
+        if (hx == 0) mbar_arrive_expect_tx(BAR(B_LX_FULL), 256);
+      }
+      ++piece;
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       float* orow = a.ws.part_o + (int64_t(s) * 128 + h) * kDc + 256 * rank;
 #pragma unroll 1
       for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
@@ -477,9 +541,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
                           __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
       }
-      if (rank == 0)
-        a.ws.part_lse[int64_t(s) * 128 + h] =
-            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       tc_fence_before();
     }
   } else if (warp >= kDequantWarp0 && kBF16) {

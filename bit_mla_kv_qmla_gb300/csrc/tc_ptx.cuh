@@ -176,6 +176,20 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, float a, float b, fl
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
       : "memory");
 }
+__device__ __forceinline__ void st_async_u32x4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c,
+                                               uint32_t d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(caddr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t caddr, float a, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   caddr),
+               "r"(__float_as_uint(a)), "r"(cluster_bar)
+               : "memory");
+}
 // 2^x with the hardware approximation (relative error about 2^-22).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
