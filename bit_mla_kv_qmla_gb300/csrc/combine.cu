@@ -17,6 +17,9 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int heads,
                                                       __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse) {
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  // launched as a programmatic dependent of the decode: wait until the
+  // decode grid has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int2 ent = ws.seq_table[b];
   const int base = ent.x, n = ent.y;
   float m = -INFINITY;
@@ -48,8 +51,20 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int heads,
 cudaError_t launch_combine(const Workspace& ws, int batch, int heads, __nv_bfloat16* out,
                            float* lse, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
-  combine_kernel<<<dim3(unsigned(batch), unsigned(heads)), 128, 0, stream>>>(ws, heads, out, lse);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the combine's CTAs may be scheduled while
+  // the decode's last CTAs finish (the decode signals early), which hides
+  // the launch latency between the two kernels.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(batch), unsigned(heads));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, ws, heads, out, lse);
 }
 
 }  // namespace qmla

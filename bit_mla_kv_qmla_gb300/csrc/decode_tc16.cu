@@ -87,7 +87,13 @@ enum : uint32_t {
 };
 constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
-constexpr uint32_t kSmBytes = kSmAbort + 12;
+// in-kernel split plan: the scanner state, this worker's pieces (slot order)
+// and its slot range
+constexpr int kPlanCap = 64;  // pieces per worker <= batch <= kPlanCap
+constexpr uint32_t kSmPlanSt = (kSmAbort + 12 + 15) & ~15u;
+constexpr uint32_t kSmPieces = (kSmPlanSt + uint32_t(sizeof(PlanState)) + 15) & ~15u;
+constexpr uint32_t kSmWr = kSmPieces + 16 * kPlanCap;
+constexpr uint32_t kSmBytes = kSmWr + 8;
 constexpr uint32_t kSmDyn = kSmBytes + 1024;
 static_assert(kSmDyn <= 232448, "shared memory budget");
 
@@ -201,12 +207,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   if (warp == kQkWarp) {
     tmem_alloc(sb0 + kSmTslot, kTmemCols);
     tmem_relinquish();
+  } else if (warp == kPvWarp && a.fused_plan) {
+    // This worker's pieces, computed here by one warp scanning seq_lens with
+    // the same functions as the planner kernel (worker 0 also publishes the
+    // per-sequence merge table).  A worker's slots are consecutive, one per
+    // sequence it touches, so they fit kPlanCap when batch <= kPlanCap.
+    PlanState& st = *reinterpret_cast<PlanState*>(sm + kSmPlanSt);
+    int4* plist = reinterpret_cast<int4*>(sm + kSmPieces);
+    const int64_t N = plan_total(a);
+    if (lane == 0) {
+      st.total_blocks = N;
+      st.carry_blocks = 0;
+      st.carry_slots = 0;
+      st.next_seq = 0;
+    }
+    __syncwarp();
+    int first = -1, cnt = 0;
+    while (plan_next(a, st, worker, worker == 0)) {
+      const int n = st.n;
+      if (n > 0) {
+        if (first < 0) first = st.list[0].slot;
+        if (lane < n) {
+          const Piece pc = st.list[lane];
+          const int k = pc.slot - first;
+          if (k >= 0 && k < kPlanCap) plist[k] = make_int4(pc.b, pc.j0, pc.j1, 0);
+        }
+        cnt += n;
+      }
+      __syncwarp();  // the next chunk rewrites st.list
+    }
+    if (lane == 0) {
+      if (cnt > kPlanCap) set_status(a.status, QMLA_STATUS_BAD_LEN);
+      *reinterpret_cast<int2*>(sm + kSmWr) =
+          (first < 0 || cnt > kPlanCap) ? make_int2(0, -1) : make_int2(first, first + cnt - 1);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kSmTslot);
-  const int2 wr = a.ws.wrange[worker];
+  // the merge kernel that follows may be scheduled now (it waits for this
+  // grid to complete before it reads anything)
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int2 wr = a.fused_plan ? *reinterpret_cast<const int2*>(sm + kSmWr) : a.ws.wrange[worker];
+  // piece s of this worker: (sequence, first block, end block)
+  const int4* plist = reinterpret_cast<const int4*>(sm + kSmPieces);
+  auto piece_at = [&](int s) -> int4 { return a.fused_plan ? plist[s - wr.x] : a.ws.pieces[s]; };
 
   if (warp == kQkWarp) {
     // ------------------------------------------------------------ QK^T issuer
@@ -220,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     uint32_t t = 0, piece = 0;
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
+      const int4 pc = piece_at(s);
       if (pc.z <= pc.y) continue;
       if (!warp_ok(mbar_wait(BAR(B_Q_FULL), piece & 1u, abort_flag, kWaitNs))) break;
       ++piece;
@@ -266,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     uint32_t t = 0;
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
+      const int4 pc = piece_at(s);
       for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
         if (!warp_ok(mbar_wait(BAR(B_P_FULL + (t & 1u)), (t >> 1) & 1u, abort_flag, kWaitNs))) {
           ok = false;
@@ -303,38 +349,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     const float c2 = a.scale * 1.4426950408889634f;
     float* red_max = reinterpret_cast<float*>(sm + kSmRed);
     float* red_sum = red_max + 4 * kH;
-    uint32_t t = 0;
-    bool ok = true;
-    for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
-      const int b = pc.x;
-      if (pc.z <= pc.y) {
-        for (int i = threadIdx.x - kSoftmaxWarp0 * 32; i < kH * kDc; i += 128)
-          a.ws.part_o[int64_t(s) * kH * kDc + i] = 0.f;
-        if (r < kH) a.ws.part_lse[int64_t(s) * kH + r] = -INFINITY;
-        continue;
-      }
-      const int L = seq_len_clamped(a, b);
-      // Q^T of this piece: 16 heads x 576 channels, binary16, SW128 K-major
-      // (the QK products of the previous piece completed before its epilogue)
-      for (int i = threadIdx.x - kSoftmaxWarp0 * 32; i < kH * 72; i += 128) {
-        const int h = i / 72, sgm = i % 72;  // 8-channel segment
+    // Q^T of sequence b: 16 heads x 576 channels, binary16, SW128 K-major.
+    // A thread's nine 16-byte segments are all loaded (q_load) before any is
+    // converted and stored (q_store), so staging waits for one load latency,
+    // and other work can run between the two halves.
+    constexpr int kSeg = kH * 72 / 128;  // 8-channel segments per thread
+    const int qi0 = threadIdx.x - kSoftmaxWarp0 * 32;
+    auto q_load = [&](int b, uint4 (&qv)[kSeg]) {
+#pragma unroll
+      for (int k = 0; k < kSeg; ++k) {
+        const int i = qi0 + 128 * k, h = i / 72, sgm = i % 72;
         const __nv_bfloat16* src =
             (sgm < 64) ? a.q_c + (int64_t(b) * kH + h) * kDc + sgm * 8
                        : a.q_r + (int64_t(b) * kH + h) * kDr + (sgm - 64) * 8;
-        const uint4 v = *reinterpret_cast<const uint4*>(src);
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        qv[k] = *reinterpret_cast<const uint4*>(src);
+      }
+    };
+    auto q_store = [&](const uint4 (&qv)[kSeg]) {
+#pragma unroll
+      for (int k = 0; k < kSeg; ++k) {
+        const int i = qi0 + 128 * k, h = i / 72, sgm = i % 72;
+        const uint32_t in[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
         uint32_t o[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xffff0000u));
+        for (int e = 0; e < 4; ++e)
+          o[e] = pack_half2(__uint_as_float(in[e] << 16), __uint_as_float(in[e] & 0xffff0000u));
         const int c = sgm >> 3, g = sgm & 7;
         unsigned char* row = sm + kSmQ + c * 2048 + (h >> 3) * 1024 + (h & 7) * 128;
         *reinterpret_cast<uint4*>(row + ((g ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       fence_proxy_async_smem();
       mbar_arrive(BAR(B_Q_FULL));
-
+    };
+    uint32_t t = 0;
+    bool ok = true;
+    bool q_staged = false;  // the current piece's Q is already in shared memory
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = piece_at(s);
+      const int b = pc.x;
+      if (pc.z <= pc.y) {
+        q_staged = false;
+        for (int i = threadIdx.x - kSoftmaxWarp0 * 32; i < kH * kDc; i += 128)
+          a.ws.part_o[int64_t(s) * kH * kDc + i] = 0.f;
+        if (r < kH) a.ws.part_lse[int64_t(s) * kH + r] = -INFINITY;
+        continue;
+      }
+      const int L = seq_len_clamped(a, b);
+      // the QK products of the previous piece completed before its epilogue
+      if (!q_staged) {
+        uint4 qv[kSeg];
+        q_load(b, qv);
+        q_store(qv);
+      }
+      const int4 pn = (s < wr.y) ? piece_at(s + 1) : make_int4(0, 0, 0, 0);  // next piece
       float m_used[kH], l_part[kH];
 #pragma unroll
       for (int h = 0; h < kH; ++h) {
@@ -344,6 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
       uint32_t vmask = 0;
       for (int jt = pc.y; jt < pc.z; jt += 2, ++t) {
         if (((jt - pc.y) & 31) == 0) vmask = valid_mask(a, b, jt, pc.z);
+        if (jt + 2 >= pc.z && pn.z > pn.y) {
+          // last tile: the next piece's queries into L2 (18 KB, 144 lines of
+          // 128 bytes), to be staged during this piece's epilogue
+          prefetch_l2(reinterpret_cast<const char*>(a.q_c + int64_t(pn.x) * kH * kDc) + 128 * qi0);
+          if (qi0 < 16)
+            prefetch_l2(reinterpret_cast<const char*>(a.q_r + int64_t(pn.x) * kH * kDr) + 128 * qi0);
+        }
         // validity of this lane's token row
         const int bi = r >> 6, jj = jt + bi;
         const bool blk_ok = jj < pc.z && ((vmask >> ((jj - pc.y) & 31)) & 1u);
@@ -473,15 +547,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
               make_float4(lsum[h], lsum[h + 1], lsum[h + 2], lsum[h + 3]);
       }
       named_bar_sync(1, 128);
+      // The next piece's queries (from L2): every QK product of this piece,
+      // the only reader of Q^T, completed before its last scores were read;
+      // the next piece's first QK then runs while the partial O is written.
+      q_staged = pn.z > pn.y;
+      if (q_staged) {
+        uint4 qv[kSeg];
+        q_load(pn.x, qv);
+        q_store(qv);
+      }
+      // 1/l with the approximate reciprocal (1 ulp): the exact one costs a
+      // long instruction sequence per head on the piece's critical path
       float inv[kH];
+      float l_r = 0.0f, m_r = 0.0f;  // row sum and maximum of head r (threads r < 16)
 #pragma unroll
       for (int h = 0; h < kH; ++h) {
         const float l = red_sum[h] + red_sum[kH + h] + red_sum[2 * kH + h] + red_sum[3 * kH + h];
-        inv[h] = l > 0.0f ? 1.0f / l : 0.0f;
-        if (r == h)
-          a.ws.part_lse[int64_t(s) * kH + h] =
-              l > 0.0f ? (m_used[h] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        inv[h] = l > 0.0f ? rcp_approx(l) : 0.0f;
+        if (r == h) {
+          l_r = l;
+          m_r = m_used[h];
+        }
       }
+      if (r < kH)
+        a.ws.part_lse[int64_t(s) * kH + r] =
+            l_r > 0.0f ? (m_r + log2f(l_r)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll 1
       for (uint32_t mk = 0; mk < 4; ++mk) {
         uint32_t o[16];
@@ -513,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     uint32_t t = 0;
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
+      const int4 pc = piece_at(s);
       if (pc.z <= pc.y) continue;
       const int L = seq_len_clamped(a, pc.x);
       const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
@@ -615,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     uint32_t t = 0;  // tiles of this worker before the current piece
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
+      const int4 pc = piece_at(s);
       if (pc.z <= pc.y) continue;
       const int L = seq_len_clamped(a, pc.x);
       const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
@@ -720,8 +810,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
 cudaError_t launch_decode_tc16(const DecodeArgs& a, cudaStream_t stream) {
   static int smem_attr_done[kMaxDevices], smem_attr_done2[kMaxDevices],
       smem_attr_done_bf16[kMaxDevices];
-  cudaError_t e = launch_plan(a, stream);
-  if (e != cudaSuccess) return e;
+  // Up to kPlanCap sequences the kernel plans its own pieces; beyond that a
+  // worker may touch more sequences than its shared-memory list holds, and
+  // the planner kernel writes the plan to the workspace instead.
+  DecodeArgs b = a;
+  b.fused_plan = a.batch <= kPlanCap ? 1 : 0;
+  cudaError_t e = cudaSuccess;
+  if (!b.fused_plan) {
+    e = launch_plan(a, stream);
+    if (e != cudaSuccess) return e;
+  }
   auto kernel = (a.fmt == QMLA_C4R4)   ? decode_tc16_kernel<4>
                 : (a.fmt == QMLA_C2R4) ? decode_tc16_kernel<2>
                                        : decode_tc16_kernel<16>;
@@ -730,7 +828,7 @@ cudaError_t launch_decode_tc16(const DecodeArgs& a, cudaStream_t stream) {
                        : a.fmt == QMLA_C2R4 ? smem_attr_done2
                                             : smem_attr_done_bf16);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3(unsigned(a.workers)), kThreads, kSmDyn, stream>>>(a);
+  kernel<<<dim3(unsigned(a.workers)), kThreads, kSmDyn, stream>>>(b);
   return cudaGetLastError();
 }
 

@@ -113,6 +113,9 @@ struct DecodeArgs {
   Workspace ws;
   int workers;  // P
   int32_t* status;
+  // The kernel plans its own pieces (no planner launch); set by the
+  // launchers that support it.
+  int fused_plan = 0;
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (the
