@@ -51,20 +51,19 @@ namespace tc {
 // and the slot range of each worker.
 __global__ void __launch_bounds__(32) plan_kernel(DecodeArgs a) {
   const int lane = threadIdx.x;
-  int64_t N = 0;
-  for (int b0 = 0; b0 < a.batch; b0 += 32) {
-    const int b = b0 + lane;
-    N += warp_sum((b < a.batch) ? seq_blocks(a, b, true) : 0);
-  }
-  const int64_t P = plan_workers(N, a.workers);  // every planned worker owns >= 1 block
-  for (int64_t w = P + lane; w < a.workers; w += 32) a.ws.wrange[w] = make_int2(0, -1);
+  const int64_t N = plan_total(a);
+  const int64_t P = plan_workers(N, a.workers);
+  // a worker that owns only piece-cost blocks (or none) has no piece
+  for (int64_t w = lane; w < a.workers; w += 32) a.ws.wrange[w] = make_int2(0, -1);
+  __syncwarp();
   int64_t carry_blocks = 0;
   int carry_slots = 0;
   for (int b0 = 0; b0 < a.batch; b0 += 32) {
     const int b = b0 + lane;
     const int nb = (b < a.batch) ? seq_blocks(a, b, false) : 0;
-    const int incl = warp_incl_scan(nb);
-    const int64_t S = carry_blocks + (incl - nb);
+    const int ext = plan_extent(a, nb);
+    const int incl = warp_incl_scan(ext);
+    const int64_t S = carry_blocks + (incl - ext) + a.piece_cost;  // first real block
     int np = 0;
     int64_t pf = 0;
     if (nb > 0) {
@@ -79,8 +78,11 @@ __global__ void __launch_bounds__(32) plan_kernel(DecodeArgs a) {
       const int64_t w0 = plan_start(w, N, P), w1 = plan_start(w + 1, N, P);
       const int j0 = int(max(w0 - S, int64_t(0))), j1 = int(min(w1 - S, int64_t(nb)));
       a.ws.pieces[base + i] = make_int4(b, j0, j1, 0);
-      if (w0 >= S) a.ws.wrange[w].x = base + i;       // the worker's first piece
-      if (w1 <= S + nb) a.ws.wrange[w].y = base + i;  // the worker's last piece
+      // the worker's first piece: its range starts inside this sequence's
+      // extent (piece cost included); its last: the range ends before the
+      // next sequence's first real block
+      if (w0 >= S - a.piece_cost) a.ws.wrange[w].x = base + i;
+      if (w1 <= S + nb + a.piece_cost) a.ws.wrange[w].y = base + i;
     }
     carry_blocks += __shfl_sync(0xffffffffu, incl, 31);
     carry_slots += __shfl_sync(0xffffffffu, np_incl, 31);

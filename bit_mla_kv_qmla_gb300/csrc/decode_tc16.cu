@@ -815,9 +815,12 @@ cudaError_t launch_decode_tc16(const DecodeArgs& a, cudaStream_t stream) {
   // the planner kernel writes the plan to the workspace instead.
   DecodeArgs b = a;
   b.fused_plan = a.batch <= kPlanCap ? 1 : 0;
+  // A second piece costs a worker about three blocks of context (the
+  // queries' staging, the pipeline refill and the epilogue).
+  b.piece_cost = 3;
   cudaError_t e = cudaSuccess;
   if (!b.fused_plan) {
-    e = launch_plan(a, stream);
+    e = launch_plan(b, stream);
     if (e != cudaSuccess) return e;
   }
   auto kernel = (a.fmt == QMLA_C4R4)   ? decode_tc16_kernel<4>

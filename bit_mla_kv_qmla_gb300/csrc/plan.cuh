@@ -4,8 +4,12 @@
 // are merged afterwards by log-sum-exp.  All sequences' 64-token blocks are
 // concatenated in sequence order and cut into min(P, N) near-equal contiguous
 // ranges, one per worker, so every worker gets the same number of blocks
-// whatever the length mix, and no planned worker is empty.  One warp scans seq_lens (32 sequences per step) with warp
-// prefix sums; no host-side copy of the lengths is needed.
+// whatever the length mix.  Optionally every non-empty sequence counts a few
+// extra blocks at its start (the piece cost), so that a worker that starts a
+// second piece, and pays for that piece's start and epilogue, gets less
+// context; a worker may then own no real block and has no piece.  One warp
+// scans seq_lens (32 sequences per step) with warp prefix sums; no host-side
+// copy of the lengths is needed.
 #pragma once
 
 #include "qmla_internal.cuh"
@@ -58,14 +62,20 @@ struct PlanState {
   Piece list[32];
 };
 
-// Called by ONE full warp: total block count N.
+// Extent of a sequence of nb blocks in the split: its blocks plus the piece
+// cost (none for an empty sequence).
+__device__ __forceinline__ int plan_extent(const DecodeArgs& a, int nb) {
+  return nb > 0 ? nb + a.piece_cost : 0;
+}
+
+// Called by ONE full warp: total extent N of all sequences.
 __device__ __forceinline__ int64_t plan_total(const DecodeArgs& a) {
   const int lane = threadIdx.x & 31;
   int64_t tot = 0;
   for (int b0 = 0; b0 < a.batch; b0 += 32) {
     const int b = b0 + lane;
     const int nb = (b < a.batch) ? seq_blocks(a, b, true) : 0;
-    tot += warp_sum(nb);
+    tot += warp_sum(plan_extent(a, nb));
   }
   return tot;
 }
@@ -84,8 +94,10 @@ __device__ __forceinline__ bool plan_next(const DecodeArgs& a, PlanState& st, in
   if (st.next_seq >= a.batch || (!publish && st.carry_blocks >= g1)) return false;
   const int b = st.next_seq + lane;
   const int nb = (b < a.batch) ? seq_blocks(a, b, false) : 0;
-  const int incl = warp_incl_scan(nb);
-  const int64_t S = st.carry_blocks + (incl - nb);
+  const int ext = plan_extent(a, nb);
+  const int incl = warp_incl_scan(ext);
+  // the sequence's real blocks start after its piece cost
+  const int64_t S = st.carry_blocks + (incl - ext) + a.piece_cost;
   int np = 0;
   int64_t pf = 0;
   if (nb > 0) {

@@ -116,6 +116,10 @@ struct DecodeArgs {
   // The kernel plans its own pieces (no planner launch); set by the
   // launchers that support it.
   int fused_plan = 0;
+  // Cost of starting a piece, in blocks: the split counts this many extra
+  // blocks at the start of every non-empty sequence, so a worker whose range
+  // crosses into another sequence gets that much less context.
+  int piece_cost = 0;
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (the

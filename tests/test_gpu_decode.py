@@ -77,6 +77,28 @@ def test_decode_large_batch_short_sequences(fmt, heads):
         compare_rows(out[b:b + 1], lse[b:b + 1], o, l, f"{fmt} H{heads} seq {b}")
 
 
+@pytest.mark.parametrize("fmt,heads", [("C4R4", 16), ("C2R4", 16), ("C4R4", 128)])
+def test_decode_many_short_sequences(fmt, heads):
+    """Up to 64 sequences (the 16-head kernel plans its own pieces) of a few
+    blocks each, with empty and one-token sequences: fewer blocks than
+    workers, so with a piece cost many workers own no real block, and every
+    worker boundary falls near a sequence start.  Every row is compared."""
+    w = W.Workload(f"short_{fmt}_{heads}", fmt, 60, heads, 200, 0, "lognormal8", 0, 29)
+    rng = np.random.default_rng(9)
+    lens = [int(x) for x in rng.integers(0, 200, 60)]
+    lens[0] = 0
+    lens[1] = 1
+    lens[2] = 64
+    lens[59] = 0
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cpu")
+    qc, qr = W.queries(w)
+    out, lse = Decoder(cache, heads, max(lens))(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    ref_o, ref_l = _oracle_full(w, cache, lens, qc, qr, "cpu")
+    compare_rows(out, lse, ref_o, ref_l, f"{fmt} H{heads} short")
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_decode_tiny_workload(fmt):
     w = W.with_format(W.WORKLOADS[0], fmt)
