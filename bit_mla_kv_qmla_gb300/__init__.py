@@ -68,6 +68,20 @@ def qmla_append(fmt, blocks, block_table, positions, latent, rope_k, status,
     _check("qmla_append", code)
 
 
+def qmla_append_advance(fmt, blocks, block_table, positions, latent, rope_k, status,
+                        stream=None) -> None:
+    """qmla_append, then positions[b] += n_new on the device (positions: int32,
+    device, written)."""
+    B, n_new = int(latent.shape[0]), int(latent.shape[1])
+    if block_table.shape[0] < B or positions.numel() < B:
+        raise ValueError("block_table / positions have fewer rows than latent")
+    num_blocks = blocks.numel() // qmla_block_bytes(fmt)
+    code = _lib.load().qmla_append_advance(
+        _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
+        _p(positions), B, n_new, _p(latent), _p(rope_k), _p(status), _stream(stream))
+    _check("qmla_append_advance", code)
+
+
 def qmla_decode_workspace_bytes(fmt, batch: int, heads: int, max_seq_len: int) -> int:
     return int(_lib.load().qmla_decode_workspace_bytes(_fmt(fmt), int(batch), int(heads),
                                                        int(max_seq_len)))

@@ -13,7 +13,8 @@ LIB_PATH = os.path.join(_PKG, "libqmla.so")
 _lib = None
 
 # exported symbols, as declared in include/qmla.h
-SYMBOLS = ("qmla_block_bytes", "qmla_append", "qmla_decode_workspace_bytes", "qmla_decode",
+SYMBOLS = ("qmla_block_bytes", "qmla_append", "qmla_append_advance",
+           "qmla_decode_workspace_bytes", "qmla_decode",
            "qmla_decode_noalloc", "qmla_read_status", "qmla_error_string")
 
 
@@ -32,6 +33,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.qmla_block_bytes.restype = sz
     L.qmla_append.argtypes = [ctypes.c_int, P, i64, P, i32, P, i32, i32, P, P, P, P]
     L.qmla_append.restype = ctypes.c_int
+    L.qmla_append_advance.argtypes = [ctypes.c_int, P, i64, P, i32, P, i32, i32, P, P, P, P]
+    L.qmla_append_advance.restype = ctypes.c_int
     L.qmla_decode_workspace_bytes.argtypes = [ctypes.c_int, i32, i32, i32]
     L.qmla_decode_workspace_bytes.restype = sz
     L.qmla_decode.argtypes = [ctypes.c_int, P, i64, P, i32, P, i32, i32, i32, P, P, f32, P, P, P,

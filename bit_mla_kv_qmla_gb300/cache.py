@@ -9,7 +9,7 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (BLOCK_TOKENS, _fmt, qmla_append, qmla_block_bytes, qmla_decode,
+from . import (BLOCK_TOKENS, _fmt, qmla_append_advance, qmla_block_bytes, qmla_decode,
                qmla_decode_workspace_bytes)
 from . import workloads as W
 
@@ -35,15 +35,14 @@ class PagedCache:
 
     def append(self, latent: torch.Tensor, rope: torch.Tensor, stream=None) -> None:
         """Append latent [B][n][512] / rope [B][n][64] (bf16, device) to every sequence."""
-        qmla_append(self.fmt, self.blocks, self.block_table, self.seq_lens, latent, rope,
-                    self.status, stream)
-        self.seq_lens += latent.shape[1]
+        qmla_append_advance(self.fmt, self.blocks, self.block_table, self.seq_lens, latent, rope,
+                            self.status, stream)
 
     def append_seq(self, b: int, latent: torch.Tensor, rope: torch.Tensor, stream=None) -> None:
         """Append latent [n][512] / rope [n][64] to sequence b only."""
-        qmla_append(self.fmt, self.blocks, self.block_table[b:b + 1], self.seq_lens[b:b + 1],
-                    latent.unsqueeze(0), rope.unsqueeze(0), self.status, stream)
-        self.seq_lens[b:b + 1] += latent.shape[0]
+        qmla_append_advance(self.fmt, self.blocks, self.block_table[b:b + 1],
+                            self.seq_lens[b:b + 1], latent.unsqueeze(0), rope.unsqueeze(0),
+                            self.status, stream)
 
 
 class Decoder:

@@ -98,11 +98,15 @@ __device__ __forceinline__ uint32_t pack_word(uint32_t c0, uint32_t c1, int bits
   return w;
 }
 
+// `advance` (one new token per sequence only): the CTA of sequence b also
+// adds 1 to positions[b] once all of its threads have read it.
 __global__ void __launch_bounds__(288) append_kernel(
     int fmt, uint8_t* __restrict__ blocks, int64_t num_blocks, const int32_t* __restrict__ table,
-    int max_blocks, const int32_t* __restrict__ positions, int n_new,
-    const __nv_bfloat16* __restrict__ latent, const __nv_bfloat16* __restrict__ rope,
-    int32_t* status) {
+    int max_blocks, int32_t* positions, int n_new, const __nv_bfloat16* __restrict__ latent,
+    const __nv_bfloat16* __restrict__ rope, int32_t* status, bool advance) {
+  // a decode launched after this kernel as a programmatic dependent may start
+  // its prologue now (it waits for this grid before reading anything)
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tok = blockIdx.x;  // b * n_new + i
   const int b = tok / n_new, i = tok % n_new;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -115,6 +119,10 @@ __global__ void __launch_bounds__(288) append_kernel(
     v = reinterpret_cast<const __nv_bfloat162*>(rope + int64_t(tok) * kDr)[lane];
   }
   const int64_t pos = int64_t(positions[b]) + i;
+  if (advance) {
+    __syncthreads();  // every thread has read positions[b]
+    if (threadIdx.x == 0) positions[b] = int32_t(pos + 1);
+  }
   const int64_t jb = pos / kT;
   if (pos < 0 || jb >= max_blocks) {
     if (threadIdx.x == 0) set_status(status, QMLA_STATUS_BAD_LEN);
@@ -170,15 +178,25 @@ __global__ void __launch_bounds__(288) append_kernel(
 
 }  // namespace
 
+__global__ void advance_kernel(int32_t* positions, int batch, int n_new) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch) positions[b] += n_new;
+}
+
 cudaError_t launch_append(int fmt, uint8_t* blocks, int64_t num_blocks, const int32_t* table,
-                          int max_blocks, const int32_t* positions, int batch, int n_new,
+                          int max_blocks, int32_t* positions, int batch, int n_new,
                           const __nv_bfloat16* latent, const __nv_bfloat16* rope,
-                          int32_t* status, cudaStream_t stream) {
+                          int32_t* status, bool advance, cudaStream_t stream) {
   const int64_t ntok = int64_t(batch) * n_new;
   if (ntok == 0) return cudaSuccess;
-  append_kernel<<<dim3(unsigned(ntok)), 288, 0, stream>>>(fmt, blocks, num_blocks, table,
-                                                         max_blocks, positions, n_new, latent,
-                                                         rope, status);
+  // one token per sequence: the append CTA advances its own position;
+  // several: a second kernel does, after every CTA has read the positions
+  const bool fused = advance && n_new == 1;
+  append_kernel<<<dim3(unsigned(ntok)), 288, 0, stream>>>(
+      fmt, blocks, num_blocks, table, max_blocks, positions, n_new, latent, rope, status, fused);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !advance || fused) return e;
+  advance_kernel<<<dim3(unsigned((batch + 255) / 256)), 256, 0, stream>>>(positions, batch, n_new);
   return cudaGetLastError();
 }
 

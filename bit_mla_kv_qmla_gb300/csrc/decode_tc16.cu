@@ -207,7 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
   if (warp == kQkWarp) {
     tmem_alloc(sb0 + kSmTslot, kTmemCols);
     tmem_relinquish();
-  } else if (warp == kPvWarp && a.fused_plan) {
+  } else if (warp == kPvWarp) {
+    // The kernel is launched as a programmatic dependent of the one before it
+    // (an append, say), so the set-up above overlaps that kernel's tail.  No
+    // thread reads global memory before this wait: the other warps read only
+    // after the barrier below.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+  if (warp == kPvWarp && a.fused_plan) {
     // This worker's pieces, computed here by one warp scanning seq_lens with
     // the same functions as the planner kernel (worker 0 also publishes the
     // per-sequence merge table).  A worker's slots are consecutive, one per
@@ -831,8 +838,17 @@ cudaError_t launch_decode_tc16(const DecodeArgs& a, cudaStream_t stream) {
                        : a.fmt == QMLA_C2R4 ? smem_attr_done2
                                             : smem_attr_done_bf16);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3(unsigned(a.workers)), kThreads, kSmDyn, stream>>>(b);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(a.workers));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmDyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, b);
 }
 
 }  // namespace qmla

@@ -32,6 +32,28 @@ int max_slots(int batch, int heads, int sms) {
   return batch + w;
 }
 
+int append_impl(int format, void* blocks, int64_t num_blocks, const int32_t* block_table,
+                int32_t max_blocks_per_seq, int32_t* positions, int32_t batch, int32_t n_new,
+                const void* latent, const void* rope_k, int32_t* status_dev, void* stream,
+                bool advance) {
+  if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
+  if (batch < 0 || n_new < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
+    return QMLA_ERR_INVALID_ARG;
+  if (int64_t(batch) * n_new == 0) return QMLA_OK;
+  if (int64_t(batch) * n_new > 0x7fffffffLL) return QMLA_ERR_CAPACITY;
+  if (!blocks || !block_table || !positions || !latent || !rope_k || !status_dev)
+    return QMLA_ERR_INVALID_ARG;
+  if (!aligned(blocks, 256) || !aligned(latent, 4) || !aligned(rope_k, 4) ||
+      !aligned(block_table, 4) || !aligned(positions, 4) || !aligned(status_dev, 4))
+    return QMLA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq == 0) return QMLA_ERR_INVALID_ARG;
+  cudaError_t e = qmla::launch_append(
+      format, static_cast<uint8_t*>(blocks), num_blocks, block_table, max_blocks_per_seq,
+      positions, batch, n_new, static_cast<const __nv_bfloat16*>(latent),
+      static_cast<const __nv_bfloat16*>(rope_k), status_dev, advance,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
+}
 }  // namespace
 
 extern "C" {
@@ -57,22 +79,18 @@ const char* qmla_error_string(int code) {
 int qmla_append(int format, void* blocks, int64_t num_blocks, const int32_t* block_table,
                 int32_t max_blocks_per_seq, const int32_t* positions, int32_t batch, int32_t n_new,
                 const void* latent, const void* rope_k, int32_t* status_dev, void* stream) {
-  if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
-  if (batch < 0 || n_new < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
-    return QMLA_ERR_INVALID_ARG;
-  if (int64_t(batch) * n_new == 0) return QMLA_OK;
-  if (int64_t(batch) * n_new > 0x7fffffffLL) return QMLA_ERR_CAPACITY;
-  if (!blocks || !block_table || !positions || !latent || !rope_k || !status_dev)
-    return QMLA_ERR_INVALID_ARG;
-  if (!aligned(blocks, 256) || !aligned(latent, 4) || !aligned(rope_k, 4) ||
-      !aligned(block_table, 4) || !aligned(positions, 4) || !aligned(status_dev, 4))
-    return QMLA_ERR_INVALID_ARG;
-  if (max_blocks_per_seq == 0) return QMLA_ERR_INVALID_ARG;
-  cudaError_t e = qmla::launch_append(
-      format, static_cast<uint8_t*>(blocks), num_blocks, block_table, max_blocks_per_seq,
-      positions, batch, n_new, static_cast<const __nv_bfloat16*>(latent),
-      static_cast<const __nv_bfloat16*>(rope_k), status_dev, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
+  // positions are only read on this path
+  return append_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq,
+                     const_cast<int32_t*>(positions), batch, n_new, latent, rope_k, status_dev,
+                     stream, false);
+}
+
+int qmla_append_advance(int format, void* blocks, int64_t num_blocks,
+                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                        int32_t* positions, int32_t batch, int32_t n_new, const void* latent,
+                        const void* rope_k, int32_t* status_dev, void* stream) {
+  return append_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, positions,
+                     batch, n_new, latent, rope_k, status_dev, stream, true);
 }
 
 size_t qmla_decode_workspace_bytes(int format, int32_t batch, int32_t heads, int32_t max_seq_len) {

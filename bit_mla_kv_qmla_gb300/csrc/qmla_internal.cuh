@@ -140,9 +140,9 @@ inline cudaError_t ensure_smem_attr(K* kernel, int bytes, int (&done)[kMaxDevice
 // Kernel launchers (each defined next to its kernel).  They return a
 // cudaError_t from the launch.
 cudaError_t launch_append(int fmt, uint8_t* blocks, int64_t num_blocks, const int32_t* table,
-                          int max_blocks, const int32_t* positions, int batch, int n_new,
+                          int max_blocks, int32_t* positions, int batch, int n_new,
                           const __nv_bfloat16* latent, const __nv_bfloat16* rope,
-                          int32_t* status, cudaStream_t stream);
+                          int32_t* status, bool advance, cudaStream_t stream);
 int simt_workers(int sms);
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
 int tc_workers(int sms, int heads);

@@ -153,6 +153,17 @@ int qmla_append(int format, void* blocks, int64_t num_blocks,
                 const void* latent, const void* rope_k,
                 int32_t* status_dev, void* stream);
 
+/* qmla_append_advance - qmla_append, then positions[b] += n_new for every
+ * sequence, on the device and in the same call (positions is written).  For
+ * a decode step (n_new = 1) this is one kernel: each sequence's CTA advances
+ * its own position once it has read it.  Errors as qmla_append; a token
+ * that is skipped for a bad slot or block id still advances its position. */
+int qmla_append_advance(int format, void* blocks, int64_t num_blocks,
+                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                        int32_t* positions, int32_t batch, int32_t n_new,
+                        const void* latent, const void* rope_k,
+                        int32_t* status_dev, void* stream);
+
 /* Workspace bytes qmla_decode needs for these sizes (split partials and the
  * per-sequence merge table); 0 for unsupported arguments. */
 size_t qmla_decode_workspace_bytes(int format, int32_t batch, int32_t heads,

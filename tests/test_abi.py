@@ -29,7 +29,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["qmla_block_bytes", "qmla_append", "qmla_decode_workspace_bytes",
+    assert names == sorted(["qmla_block_bytes", "qmla_append", "qmla_append_advance",
+                            "qmla_decode_workspace_bytes",
                             "qmla_decode", "qmla_decode_noalloc", "qmla_read_status",
                             "qmla_error_string"])
 
@@ -61,16 +62,17 @@ def _fake(n):
     return buf, addr
 
 
-def test_append_rejects_bad_arguments(lib):
+@pytest.mark.parametrize("entry", ["qmla_append", "qmla_append_advance"])
+def test_append_rejects_bad_arguments(lib, entry):
     keep, p = _fake(1024)
     ok_args = dict(format=0, blocks=p, num_blocks=4, table=p, maxb=2, pos=p, batch=1, n_new=1,
                    lat=p, rope=p, status=p, stream=None)
+    fn = getattr(lib, entry)
 
     def call(**kw):
         a = dict(ok_args, **kw)
-        return lib.qmla_append(a["format"], a["blocks"], a["num_blocks"], a["table"], a["maxb"],
-                               a["pos"], a["batch"], a["n_new"], a["lat"], a["rope"], a["status"],
-                               a["stream"])
+        return fn(a["format"], a["blocks"], a["num_blocks"], a["table"], a["maxb"], a["pos"],
+                  a["batch"], a["n_new"], a["lat"], a["rope"], a["status"], a["stream"])
     assert call(format=7) == -2
     assert call(batch=-1) == -1
     assert call(n_new=-1) == -1

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from bit_mla_kv_qmla_gb300 import (QMLA_STATUS_BAD_BLOCK, QMLA_STATUS_BAD_LEN, qmla_append,
-                                   qmla_block_bytes)
+                                   qmla_append_advance, qmla_block_bytes)
 from bit_mla_kv_qmla_gb300 import workloads as W
 from bit_mla_kv_qmla_gb300.cache import PagedCache, build_cache
 
@@ -147,3 +147,28 @@ def test_append_out_of_range_is_flagged_not_faulted():
     torch.cuda.synchronize()
     assert status.item() & QMLA_STATUS_BAD_LEN
     assert torch.count_nonzero(blocks[bb:]) == 0
+
+
+@pytest.mark.parametrize("n_new", [1, 5])
+def test_append_advance_matches_append(n_new):
+    """qmla_append_advance writes the same bytes as qmla_append and advances
+    every position by n_new (one kernel for n_new = 1, two otherwise),
+    including a sequence whose block id is out of range."""
+    B = 4
+    g = torch.Generator().manual_seed(17)
+    lat = torch.randn(B, n_new, 512, generator=g).to(torch.bfloat16).cuda()
+    rope = torch.randn(B, n_new, 64, generator=g).to(torch.bfloat16).cuda()
+    table = torch.tensor([[0, 1], [2, 3], [4, 5], [9, 9]], dtype=torch.int32, device="cuda")
+    pos0 = torch.tensor([0, 61, 63, 0], dtype=torch.int32, device="cuda")
+    bb = qmla_block_bytes("C4R4")
+    ref_blocks = torch.zeros(6 * bb, dtype=torch.uint8, device="cuda")
+    ref_status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qmla_append("C4R4", ref_blocks, table, pos0, lat, rope, ref_status)
+    blocks = torch.zeros_like(ref_blocks)
+    status = torch.zeros_like(ref_status)
+    pos = pos0.clone()
+    qmla_append_advance("C4R4", blocks, table, pos, lat, rope, status)
+    torch.cuda.synchronize()
+    assert torch.equal(blocks, ref_blocks)
+    assert torch.equal(pos, pos0 + n_new)
+    assert status.item() == ref_status.item() and status.item() & QMLA_STATUS_BAD_BLOCK
