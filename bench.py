@@ -280,8 +280,33 @@ def run_ours(args, rank, world, device):
             h_lse.copy_(lse, non_blocking=True)
             torch.cuda.current_stream(device).synchronize()
 
+        if use_graph:
+            # The same calls captured once per cache copy (copies included)
+            # and replayed: a user who issues this step repeatedly does the
+            # same, and the host then waits for the result each step.
+            g_e2e = []
+            for i in range(copies):
+                ge = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(ge):
+                    if n_app:
+                        d_lat.copy_(h_lat, non_blocking=True)
+                        d_rope.copy_(h_rope, non_blocking=True)
+                        caches[i].append(d_lat[:, :n_app], d_rope[:, :n_app])
+                    d_qc.copy_(h_qc, non_blocking=True)
+                    d_qr.copy_(h_qr, non_blocking=True)
+                    out, lse = decs[i](d_qc, d_qr, w.scale)
+                    h_out.copy_(out, non_blocking=True)
+                    h_lse.copy_(lse, non_blocking=True)
+                g_e2e.append(ge)
+            torch.cuda.synchronize(device)
+
+            def e2e_step(i):  # noqa: F811
+                g_e2e[i].replay()
+                torch.cuda.current_stream(device).synchronize()
+
         for k in range(3):
             e2e_step(k % copies)
+            lens_at[k % copies] = [L + n_app for L in lens_at[k % copies]]
         tok_e2e = 0
         s0 = time.perf_counter()
         for k in range(args.e2e_steps):
@@ -292,7 +317,8 @@ def run_ours(args, rank, world, device):
         e2e_t = time.perf_counter() - s0
         e2e = {"value": tok_e2e / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-               "ms_per_step": 1e3 * e2e_t / args.e2e_steps}
+               "ms_per_step": 1e3 * e2e_t / args.e2e_steps,
+               "issue": "CUDA graph replay" if use_graph else "eager calls"}
 
     lens_mid = [L for L in lens_at[0]]
     pk = peaks()
