@@ -2,7 +2,8 @@
 //
 // Each piece i of a sequence holds a normalized partial O_i and its LSE_i;
 // the full result is LSE = ln sum_i exp(LSE_i) and
-// O = sum_i exp(LSE_i - LSE) * O_i, written as bfloat16 O and binary32 LSE.
+// O = sum_i exp(LSE_i - LSE) * O_i, written as bfloat16 O and binary32 LSE
+// (computed as sum_i w_i O_i / sum_i w_i with w_i = exp(LSE_i - max_j LSE_j)).
 // A sequence with no piece (length 0) gets O = 0 and LSE = -inf.
 // Grid (batch, heads), 128 threads, 4 channels per thread.
 
@@ -22,23 +23,34 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int heads,
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int2 ent = ws.seq_table[b];
   const int base = ent.x, n = ent.y;
+  const float* plse = ws.part_lse + int64_t(base) * heads + h;
+  const float4* po = reinterpret_cast<const float4*>(ws.part_o + (int64_t(base) * heads + h) * kDc) + tid;
+  const int64_t ostride = int64_t(heads) * kDc / 4;  // float4s from one piece to the next
+  // two passes, each unrolled so that several pieces' loads are in flight:
+  // the maximum LSE, then the weighted sum of the partial outputs
   float m = -INFINITY;
-  for (int i = 0; i < n; ++i) m = fmaxf(m, ws.part_lse[int64_t(base + i) * heads + h]);
+#pragma unroll 4
+  for (int i = 0; i < n; ++i) m = fmaxf(m, plse[int64_t(i) * heads]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = -INFINITY;
   if (m > -INFINITY) {
     float sum = 0.0f;
-    for (int i = 0; i < n; ++i) sum += __expf(ws.part_lse[int64_t(base + i) * heads + h] - m);
-    L = m + logf(sum);
+#pragma unroll 4
     for (int i = 0; i < n; ++i) {
-      const float wgt = __expf(ws.part_lse[int64_t(base + i) * heads + h] - L);
-      const float4 o = reinterpret_cast<const float4*>(
-          ws.part_o + (int64_t(base + i) * heads + h) * kDc)[tid];
+      const float wgt = __expf(plse[int64_t(i) * heads] - m);
+      const float4 o = po[int64_t(i) * ostride];
+      sum += wgt;
       acc.x = fmaf(wgt, o.x, acc.x);
       acc.y = fmaf(wgt, o.y, acc.y);
       acc.z = fmaf(wgt, o.z, acc.z);
       acc.w = fmaf(wgt, o.w, acc.w);
     }
+    const float inv = 1.0f / sum;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    L = m + logf(sum);
   }
   __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + (int64_t(b) * heads + h) * kDc) + 2 * tid;
   dst[0] = __floats2bfloat162_rn(acc.x, acc.y);

@@ -98,10 +98,11 @@ constexpr uint32_t kSmDyn = kSmBytes + 1024;
 static_assert(kSmDyn <= 232448, "shared memory budget");
 
 // Packed codes of one half-tile for one dequantization thread: two content
-// groups (codes and scale/zero) and 16 RoPE channels (codes, scale/zero).
+// groups (codes and scale/zero) and, in the first half, 32 RoPE channels
+// (codes, scale/zero).
 struct HalfCodes {
   uint32_t c0[8], c1[8];
-  uint32_t sz0, sz1, rope0, rope1, rsz;
+  uint32_t sz0, sz1, rope[4], rsz;
 };
 __device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* r) {
   asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -143,8 +144,10 @@ __device__ __forceinline__ void load_half(HalfCodes& L, const uint8_t* blk, cons
   }
   L.sz0 = ld_nc_b32(half + G.sz_off + (g0 * 64 + tt) * 4);
   L.sz1 = ld_nc_b32(half + G.sz_off + ((g0 + 1) * 64 + tt) * 4);
-  ld_nc_v2(half + G.rope_off + tt * 16 + dw * 8, L.rope0, L.rope1);
-  L.rsz = ld_nc_b32(blk + G.rope_sz_off + tt * 4);
+  if (h == 0) {  // RoPE channels 32dw .. 32dw+31: the RoPE words of block half dw
+    ld_nc_v4(blk + dw * G.half + G.rope_off + tt * 16, L.rope);
+    L.rsz = ld_nc_b32(blk + G.rope_sz_off + tt * 4);
+  }
 }
 // Channels 32*part .. 32*part+31 of one content group as 16 words of
 // binary16 pairs (channel 2k low, 2k+1 high).
@@ -296,10 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
             mma_ts_warp(tbase + kColS + kH * ks, tbase + kColK + 32 * c + 8 * ks,
                         dQ + ((c * 2048 + 32 * ks) >> 4), idesc, c > 0 ? 1u : 0u);
           }
+          // RoPE: the low-bit dequantization writes all of it with half 0
+          // (half 1 is the one on the critical path), the BF16 one half each
+          constexpr uint32_t kRopeSteps = kBF16 ? 2 : 4;
+          if (kBF16 || h == 0) {
 #pragma unroll
-          for (uint32_t ks = 2 * h; ks < 2 * h + 2; ++ks)
-            mma_ts_warp(tbase + kColS + kH * ks, tbase + kColRope + 8 * ks,
-                        dQ + ((8 * 2048 + 32 * ks) >> 4), idesc, 1u);
+            for (uint32_t ks = kBF16 ? 2 * h : 0; ks < (kBF16 ? 2 * h : 0) + kRopeSteps; ++ks)
+              mma_ts_warp(tbase + kColS + kH * ks, tbase + kColRope + 8 * ks,
+                          dQ + ((8 * 2048 + 32 * ks) >> 4), idesc, 1u);
+          }
           mma_commit_warp(BAR(B_K_EMPTY + h));
         }
         if (!ok) break;
@@ -701,9 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
     // warp: lane quarter q (tensor-memory lanes 32q..32q+31 = token rows) and
     // column half dw.  Rows 0-63 come from the tile's first block, 64-127 from
     // its second.  For half h the warp dequantizes content groups 4h+2dw and
-    // 4h+2dw+1 and RoPE channels 32h+16dw .. 32h+16dw+15 of its tokens.  The
-    // loads of the next half-tile of the piece are issued before the current
-    // one is processed.
+    // 4h+2dw+1 of its tokens, and with half 0 also RoPE channels 32dw ..
+    // 32dw+31, which keeps half 1 -- the half that waits for the previous
+    // tile's P.V and holds up this tile's QK -- short.  The loads of the next
+    // half-tile of the piece are issued before the current one is processed.
     const int q = warp & 3, dw = (warp - kDequantWarp0) >> 2;
     const int r = 32 * q + lane, bi = q >> 1, tt = r & 63;
     const uint32_t lane_base = uint32_t(32 * q) << 16;
@@ -781,14 +790,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
                     make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
             }
           }
-          {
-            // RoPE channels 32h+16dw .. +15 (INT4)
+          if (h == 0) {
+            // RoPE channels 32dw .. 32dw+31 (INT4)
             __half2 s2, z2;
             split_sz(cur.rsz, s2, z2);
-            uint32_t v[8];
-            dq_int4(cur.rope0, s2, z2, v);
-            dq_int4(cur.rope1, s2, z2, v + 4);
-            tmem_st8(tbase + lane_base + kColRope + 16 * h + 8 * dw, v);
+            uint32_t v[16];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) dq_int4(cur.rope[w], s2, z2, v + 4 * w);
+            tmem_st16(tbase + lane_base + kColRope + 16 * dw, v);
           }
           tmem_wait_st();
           fence_proxy_async_smem();
