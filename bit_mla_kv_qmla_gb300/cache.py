@@ -57,8 +57,13 @@ class Decoder:
         if nbytes == 0:
             raise ValueError("unsupported decode shape")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        self.out = torch.empty(cache.batch, heads, W.D_C, dtype=torch.bfloat16, device=dev)
-        self.lse = torch.empty(cache.batch, heads, dtype=torch.float32, device=dev)
+        # out and lse in one allocation (lse 256-byte aligned after out), so a
+        # caller can read the step's result back with a single copy of `io`
+        ob = cache.batch * heads * W.D_C * 2
+        lo = (ob + 255) // 256 * 256
+        self.io = torch.empty(lo + cache.batch * heads * 4, dtype=torch.uint8, device=dev)
+        self.out = self.io[:ob].view(torch.bfloat16).view(cache.batch, heads, W.D_C)
+        self.lse = self.io[lo:].view(torch.float32).view(cache.batch, heads)
 
     def __call__(self, q_c: torch.Tensor, q_r: torch.Tensor, scale: float, stream=None):
         c = self.cache
