@@ -143,6 +143,22 @@ def roofline_for(fmt, heads, lens, t_s, pk, traffic):
             "peak_note": "f16 operands: same nominal dense rate as bf16"}
 
 
+def step_launches(w, n_app, tc):
+    """Library kernels one step launches: decode and merge; the planner
+    kernel too for the 128-head kernel and for the 16-head one above 64
+    sequences (it plans for itself up to there; the CUDA-core kernel always
+    does); the append (advancing the lengths itself for one token, with a
+    second kernel for several)."""
+    k = 2
+    if tc and (w.heads != 16 or w.batch > 64):
+        k += 1
+    if n_app == 1:
+        k += 1
+    elif n_app > 1:
+        k += 2
+    return k
+
+
 def run_ours(args, rank, world, device):
     import torch
     import bit_mla_kv_qmla_gb300 as q
@@ -337,7 +353,7 @@ def run_ours(args, rank, world, device):
            "dtype": "f16" if tc else "f32",
            "clocks": clocks, "e2e": e2e, "workload": w, "copies": copies,
            "cache_bytes": cache_bytes,
-           "launches": args.steps * ((1 if n_app else 0) + (3 if tc else 2)),
+           "launches": args.steps * step_launches(w, n_app, tc),
            "graph": use_graph}
     return res
 
