@@ -237,3 +237,27 @@ def merge(part_o: np.ndarray, part_lse: np.ndarray):
     lse = np.zeros(H, np.float64)
     lib().oracle_merge(n, H, _ptr(po), _ptr(pl), _ptr(out), _ptr(lse))
     return out, lse
+
+
+def decode_multi(fmt: int, blocks: np.ndarray, block_table: np.ndarray, seq_lens: np.ndarray,
+                 q_c, q_r, scale: float):
+    """Decode of q_len query tokens per sequence, the last q_len tokens of the
+    cache (q_c [B][q_len][H][512], q_r [B][q_len][H][64]).  Query i sits at
+    position L - q_len + i and attends causally: to tokens 0 .. L - q_len + i,
+    i.e. the decode over the first L - q_len + 1 + i tokens (none when that is
+    not positive: O = 0, LSE = -inf).  Returns (O [B][q_len][H][512],
+    LSE [B][q_len][H]) in float64.  The multi-token query step is not in the
+    pages; it is plain causal attention over the same cache, so it reuses
+    ``decode`` on each query's prefix."""
+    qc = _u16(q_c)
+    qr = _u16(q_r)
+    B, Q, H = qc.shape[0], qc.shape[1], qc.shape[2]
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    out = np.zeros((B, Q, H, D_C), np.float64)
+    lse = np.full((B, Q, H), -np.inf, np.float64)
+    for i in range(Q):
+        li = np.maximum(lens - (Q - 1 - i), 0).astype(np.int32)
+        o, l = decode(fmt, blocks, block_table, li, qc[:, i], qr[:, i], scale)
+        out[:, i] = o
+        lse[:, i] = l
+    return out, lse

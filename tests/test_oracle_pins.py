@@ -526,3 +526,31 @@ def test_merge_matches_logaddexp():
     assert np.allclose(lse, L, atol=1e-12)
     w = np.exp(pl - L)
     assert np.allclose(O, np.einsum("nh,nhc->hc", w, po), atol=1e-12)
+
+
+def test_decode_multi_matches_explicit_causal_mask():
+    """The multi-token query decode against its textbook form: the full score
+    matrix of every query against every cached token, with the causal mask
+    (query i at position L - q_len + i sees tokens up to it) applied before a
+    library softmax; a sequence shorter than q_len leaves its first queries
+    with nothing to attend (O = 0, LSE = -inf)."""
+    from scipy.special import logsumexp, softmax
+    B, Q, H, lens = 3, 3, 2, [70, 5, 1]
+    lat, rope = _rand((B, 70, 512), 11), _rand((B, 70, 64), 12)
+    qc, qr = _rand((B, Q, H, 512), 13), _rand((B, Q, H, 64), 14)
+    blocks, table = _build_cache(oracle.BF16, lat, rope, lens)
+    scale = 1 / math.sqrt(192)
+    O, lse = oracle.decode_multi(oracle.BF16, blocks, table, np.array(lens), qc, qr, scale)
+    for b, L in enumerate(lens):
+        K = np.concatenate([lat[b, :L].double().numpy(), rope[b, :L].double().numpy()], 1)
+        for i in range(Q):
+            pos = L - Q + i  # position of query i
+            Qm = np.concatenate([qc[b, i].double().numpy(), qr[b, i].double().numpy()], 1)
+            S = (Qm @ K.T) * scale
+            S[:, np.arange(L) > pos] = -np.inf
+            if pos < 0:
+                assert np.all(O[b, i] == 0) and np.all(np.isneginf(lse[b, i]))
+                continue
+            assert np.allclose(lse[b, i], logsumexp(S, axis=1), rtol=0, atol=1e-12)
+            ref = softmax(S, axis=1) @ lat[b, :L].double().numpy()
+            assert np.allclose(O[b, i], ref, rtol=0, atol=1e-12)
