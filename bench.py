@@ -392,7 +392,57 @@ def measure_also(args, device):
                        "cache_bytes": cache.blocks.numel()}
         del cache, dec, flush
         torch.cuda.empty_cache()
+    out.update(measure_multi(device, pk))
     return out
+
+
+def measure_multi(device, pk):
+    """Multi-token query decode (qmla_decode_multi) on the 32 x 8K C4R4 cache
+    with 16 heads and 8 query tokens per sequence: 128 query rows per
+    sequence on the 128-head tensor-core kernel.  tokens_per_s counts every
+    query's visible tokens; the roofline counts the cache once and the
+    tensor work of every (query row, visible token)."""
+    import torch
+    from bit_mla_kv_qmla_gb300 import workloads as W
+    from bit_mla_kv_qmla_gb300.cache import Decoder, build_cache
+    w = W.WORKLOADS[1]
+    q_len = 8
+    lens = W.seq_lens(w)
+    cache = build_cache(w, device)
+    dec = Decoder(cache, w.heads, max(lens), q_len=q_len)
+    g = torch.Generator(device=device)
+    g.manual_seed(77)
+    qc = torch.randn(w.batch, q_len, w.heads, 512, generator=g, device=device).to(torch.bfloat16)
+    qr = torch.randn(w.batch, q_len, w.heads, 64, generator=g, device=device).to(torch.bfloat16)
+    for _ in range(3):
+        dec(qc, qr, w.scale)
+    torch.cuda.synchronize(device)
+    n = 10
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    for a, b in evs:
+        flush.fill_(1.0)
+        a.record()
+        dec(qc, qr, w.scale)
+        b.record()
+    torch.cuda.synchronize(device)
+    assert cache.status.item() == 0
+    t = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+    seen = sum(max(0, L - (q_len - 1 - i)) for L in lens for i in range(q_len))
+    flops = seen * w.heads * FLOP_PER_TOKEN_HEAD
+    bytes_alg = sum(lens) * TOKEN_BYTES["C4R4"] + w.batch * q_len * w.heads * IO_BYTES_PER_HEAD
+    t_mem = bytes_alg / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    roof = ({"bound": "tensor", "achieved": round(flops / t / 1e12, 1), "unit": "TFLOP/s"}
+            if t_tc > t_mem else
+            {"bound": "hbm", "achieved": round(bytes_alg / t / 1e9, 1), "unit": "GB/s"})
+    roof["frac"] = round(max(t_mem, t_tc) / t, 4)
+    res = {"tokens_per_s": seen / t, "decode_us": round(t * 1e6, 2), "q_len": q_len,
+           "query_rows": w.heads * q_len, "roofline": roof}
+    del cache, dec, flush
+    torch.cuda.empty_cache()
+    return {f"c4r4_b32_h16x{q_len}_l8192_multiquery": res}
 
 
 def footprint_sweep():

@@ -104,6 +104,25 @@ def qmla_decode(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r, 
     _check("qmla_decode", code)
 
 
+def qmla_decode_multi(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r,
+                      scale: float, out, lse, workspace, status, stream=None) -> None:
+    """Decode of q_len query tokens per sequence with a causal mask: q_c
+    [B][q_len][H][512], q_r [B][q_len][H][64]; writes out [B][q_len][H][512]
+    bf16 and lse [B][q_len][H] f32."""
+    B, Q, H = int(q_c.shape[0]), int(q_c.shape[1]), int(q_c.shape[2])
+    if block_table.shape[0] < B or seq_lens.numel() < B or tuple(q_r.shape[:3]) != (B, Q, H):
+        raise ValueError("block_table / seq_lens / q_r do not cover the query batch")
+    if tuple(out.shape) != (B, Q, H, D_C) or tuple(lse.shape) != (B, Q, H):
+        raise ValueError("out / lse shapes do not match the queries")
+    num_blocks = blocks.numel() // qmla_block_bytes(fmt)
+    code = _lib.load().qmla_decode_multi(
+        _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
+        _p(seq_lens), int(max_seq_len), B, H, Q, _p(q_c), _p(q_r), float(scale), _p(out),
+        _p(lse), _p(workspace), int(workspace.numel() * workspace.element_size()), _p(status),
+        _stream(stream))
+    _check("qmla_decode_multi", code)
+
+
 def qmla_decode_noalloc(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r,
                         scale: float, out, lse, status, stream=None) -> None:
     """qmla_decode without a workspace argument, for callers that cannot

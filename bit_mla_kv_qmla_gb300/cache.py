@@ -10,7 +10,7 @@ from typing import Optional, Sequence
 import torch
 
 from . import (BLOCK_TOKENS, _fmt, qmla_append_advance, qmla_block_bytes, qmla_decode,
-               qmla_decode_workspace_bytes)
+               qmla_decode_multi, qmla_decode_workspace_bytes)
 from . import workloads as W
 
 
@@ -46,29 +46,35 @@ class PagedCache:
 
 
 class Decoder:
-    """Pre-allocated outputs and workspace for repeated qmla_decode calls."""
+    """Pre-allocated outputs and workspace for repeated qmla_decode calls
+    (q_len > 1: qmla_decode_multi, q_len query tokens per sequence)."""
 
-    def __init__(self, cache: PagedCache, heads: int, max_seq_len: int):
+    def __init__(self, cache: PagedCache, heads: int, max_seq_len: int, q_len: int = 1):
         self.cache = cache
         self.heads = heads
+        self.q_len = int(q_len)
         self.max_seq_len = int(max_seq_len)
         dev = cache.device
-        nbytes = qmla_decode_workspace_bytes(cache.fmt, cache.batch, heads, self.max_seq_len)
+        nbytes = qmla_decode_workspace_bytes(cache.fmt, cache.batch, heads * self.q_len,
+                                             self.max_seq_len)
         if nbytes == 0:
             raise ValueError("unsupported decode shape")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         # out and lse in one allocation (lse 256-byte aligned after out), so a
         # caller can read the step's result back with a single copy of `io`
-        ob = cache.batch * heads * W.D_C * 2
+        rows = heads * self.q_len
+        ob = cache.batch * rows * W.D_C * 2
         lo = (ob + 255) // 256 * 256
-        self.io = torch.empty(lo + cache.batch * heads * 4, dtype=torch.uint8, device=dev)
-        self.out = self.io[:ob].view(torch.bfloat16).view(cache.batch, heads, W.D_C)
-        self.lse = self.io[lo:].view(torch.float32).view(cache.batch, heads)
+        self.io = torch.empty(lo + cache.batch * rows * 4, dtype=torch.uint8, device=dev)
+        shape = (cache.batch, heads) if self.q_len == 1 else (cache.batch, self.q_len, heads)
+        self.out = self.io[:ob].view(torch.bfloat16).view(*shape, W.D_C)
+        self.lse = self.io[lo:].view(torch.float32).view(*shape)
 
     def __call__(self, q_c: torch.Tensor, q_r: torch.Tensor, scale: float, stream=None):
         c = self.cache
-        qmla_decode(c.fmt, c.blocks, c.block_table, c.seq_lens, self.max_seq_len, q_c, q_r,
-                    scale, self.out, self.lse, self.workspace, c.status, stream)
+        fn = qmla_decode if self.q_len == 1 else qmla_decode_multi
+        fn(c.fmt, c.blocks, c.block_table, c.seq_lens, self.max_seq_len, q_c, q_r, scale,
+           self.out, self.lse, self.workspace, c.status, stream)
         return self.out, self.lse
 
 

@@ -173,8 +173,11 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
               s0 = fmaf(qv, S.x[tl][c], s0);
               s1 = fmaf(qv, S.x[tl + 16][c], s1);
             }
-            S.p[tl][h] = (tl < nv) ? s0 * a.scale : -INFINITY;
-            S.p[tl + 16][h] = (tl + 16 < nv) ? s1 * a.scale : -INFINITY;
+            // tokens virtual head hg*kHG+h may see (a prefix of them in a
+            // multi-token query decode)
+            const int vis = visible_tokens(a, hg * kHG + h, L) - (j * kT + t0);
+            S.p[tl][h] = (tl < nv && tl < vis) ? s0 * a.scale : -INFINITY;
+            S.p[tl + 16][h] = (tl + 16 < nv && tl + 16 < vis) ? s1 * a.scale : -INFINITY;
           }
           __syncthreads();
           // 3. online softmax: warp handles heads 2*warp, 2*warp+1; lane = token
@@ -186,15 +189,16 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
             const float m_old = S.m[h];
-            const float m_new = fmaxf(m_old, mt);  // finite: at least one valid token
-            const float p = __expf(v - m_new);
+            // -inf only while a multi-token query's head has seen no token
+            const float m_new = fmaxf(m_old, mt);
+            const float p = m_new == -INFINITY ? 0.0f : __expf(v - m_new);
             float ps = p;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
             __syncwarp();
             S.p[lane][h] = p;
             if (lane == 0) {
-              const float al = __expf(m_old - m_new);
+              const float al = m_new == -INFINITY ? 1.0f : __expf(m_old - m_new);
               S.alpha[h] = al;
               S.m[h] = m_new;
               S.l[h] = S.l[h] * al + ps;

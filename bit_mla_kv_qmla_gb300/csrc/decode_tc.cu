@@ -441,7 +441,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (hx == 0) mbar_arrive_expect_tx(BAR(B_X_FULL + sb), kX);
           mbar_arrive_remote(mapa(BAR(B_X_EMPTY + sb), peer));
 
-          const int nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
+          // tokens of this tile head h may see (its query's prefix in a
+          // multi-token query decode)
+          const int nvalid =
+              ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, visible_tokens(a, h, L) - j * kT) : 0;
 #pragma unroll
           for (int i = 0; i < 64; ++i) sv[i] *= c2;
           if (nvalid < 64) {

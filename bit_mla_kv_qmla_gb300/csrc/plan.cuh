@@ -47,6 +47,12 @@ __device__ __forceinline__ int seq_len_clamped(const DecodeArgs& a, int b) {
   return max(0, min(a.seq_lens[b], cap));
 }
 
+// Cached tokens virtual head v attends to in a sequence of L tokens (a prefix
+// of them in a multi-token query decode; possibly <= 0: none).
+__device__ __forceinline__ int visible_tokens(const DecodeArgs& a, int v, int L) {
+  return a.q_heads > 0 ? L - (a.q_len - 1 - v / a.q_heads) : L;
+}
+
 // One piece of work: blocks [j0, j1) of sequence b, partial result to `slot`.
 struct Piece {
   int b, j0, j1, slot;

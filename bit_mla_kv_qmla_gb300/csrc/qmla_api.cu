@@ -54,6 +54,65 @@ int append_impl(int format, void* blocks, int64_t num_blocks, const int32_t* blo
       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
 }
+// The decode; q_len > 1: `heads` is q_len * q_heads virtual heads of a
+// multi-token query step (qmla_decode_multi).
+int decode_impl(int format, const void* blocks, int64_t num_blocks, const int32_t* block_table,
+                int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                int32_t batch, int32_t heads, int32_t q_len, int32_t q_heads, const void* q_c,
+                const void* q_r, float softmax_scale, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
+  if (batch < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
+    return QMLA_ERR_INVALID_ARG;
+  if (!heads_served(format, heads)) return QMLA_ERR_UNSUPPORTED;
+  if (batch == 0) return QMLA_OK;
+  if (!blocks || !block_table || !seq_lens || !q_c || !q_r || !out || !lse || !workspace ||
+      !status_dev)
+    return QMLA_ERR_INVALID_ARG;
+  if (!aligned(blocks, 256) || !aligned(workspace, 256) || !aligned(q_c, 16) ||
+      !aligned(q_r, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(seq_lens, 4) ||
+      !aligned(block_table, 4) || !aligned(status_dev, 4))
+    return QMLA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq == 0) return QMLA_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return QMLA_ERR_CUDA;
+  const int slots = max_slots(batch, heads, sms);
+  if (workspace_bytes < qmla::workspace_bytes(batch, heads, slots)) return QMLA_ERR_WORKSPACE;
+
+  qmla::DecodeArgs a;
+  a.fmt = format;
+  a.blocks = static_cast<const uint8_t*>(blocks);
+  a.num_blocks = num_blocks;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.seq_lens = seq_lens;
+  a.max_seq_len = max_seq_len;
+  a.batch = batch;
+  a.heads = heads;
+  a.q_c = static_cast<const __nv_bfloat16*>(q_c);
+  a.q_r = static_cast<const __nv_bfloat16*>(q_r);
+  a.scale = softmax_scale;
+  a.ws = qmla::carve(workspace, batch, heads, slots);
+  a.status = status_dev;
+  a.q_len = q_len;
+  a.q_heads = q_len > 1 ? q_heads : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // 16 query rows of a multi-token query step go to the CUDA-core kernel:
+  // the 16-head tensor-core kernel has no causal mask (it would cost the
+  // single-token decode its hot loop's room)
+  if (qmla::tc_supported(format, heads) && !(q_len > 1 && heads == 16)) {
+    a.workers = qmla::tc_workers(sms, heads);
+    e = qmla::launch_decode_tc(a, s);
+  } else {
+    a.workers = qmla::simt_workers(sms);
+    e = qmla::launch_decode_simt(a, s);
+  }
+  if (e != cudaSuccess) return QMLA_ERR_CUDA;
+  e = qmla::launch_combine(a.ws, batch, heads, static_cast<__nv_bfloat16*>(out), lse, s);
+  return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -106,51 +165,21 @@ int qmla_decode(int format, const void* blocks, int64_t num_blocks, const int32_
                 int32_t batch, int32_t heads, const void* q_c, const void* q_r,
                 float softmax_scale, void* out, float* lse, void* workspace,
                 size_t workspace_bytes, int32_t* status_dev, void* stream) {
-  if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
-  if (batch < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
-    return QMLA_ERR_INVALID_ARG;
-  if (!heads_served(format, heads)) return QMLA_ERR_UNSUPPORTED;
-  if (batch == 0) return QMLA_OK;
-  if (!blocks || !block_table || !seq_lens || !q_c || !q_r || !out || !lse || !workspace ||
-      !status_dev)
-    return QMLA_ERR_INVALID_ARG;
-  if (!aligned(blocks, 256) || !aligned(workspace, 256) || !aligned(q_c, 16) ||
-      !aligned(q_r, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(seq_lens, 4) ||
-      !aligned(block_table, 4) || !aligned(status_dev, 4))
-    return QMLA_ERR_INVALID_ARG;
-  if (max_blocks_per_seq == 0) return QMLA_ERR_INVALID_ARG;
-  const int sms = device_sms();
-  if (sms <= 0) return QMLA_ERR_CUDA;
-  const int slots = max_slots(batch, heads, sms);
-  if (workspace_bytes < qmla::workspace_bytes(batch, heads, slots)) return QMLA_ERR_WORKSPACE;
+  return decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
+                     max_seq_len, batch, heads, 1, 0, q_c, q_r, softmax_scale, out, lse,
+                     workspace, workspace_bytes, status_dev, stream);
+}
 
-  qmla::DecodeArgs a;
-  a.fmt = format;
-  a.blocks = static_cast<const uint8_t*>(blocks);
-  a.num_blocks = num_blocks;
-  a.block_table = block_table;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.seq_lens = seq_lens;
-  a.max_seq_len = max_seq_len;
-  a.batch = batch;
-  a.heads = heads;
-  a.q_c = static_cast<const __nv_bfloat16*>(q_c);
-  a.q_r = static_cast<const __nv_bfloat16*>(q_r);
-  a.scale = softmax_scale;
-  a.ws = qmla::carve(workspace, batch, heads, slots);
-  a.status = status_dev;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (qmla::tc_supported(format, heads)) {
-    a.workers = qmla::tc_workers(sms, heads);
-    e = qmla::launch_decode_tc(a, s);
-  } else {
-    a.workers = qmla::simt_workers(sms);
-    e = qmla::launch_decode_simt(a, s);
-  }
-  if (e != cudaSuccess) return QMLA_ERR_CUDA;
-  e = qmla::launch_combine(a.ws, batch, heads, static_cast<__nv_bfloat16*>(out), lse, s);
-  return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
+int qmla_decode_multi(int format, const void* blocks, int64_t num_blocks,
+                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                      const int32_t* seq_lens, int32_t max_seq_len, int32_t batch, int32_t heads,
+                      int32_t q_len, const void* q_c, const void* q_r, float softmax_scale,
+                      void* out, float* lse, void* workspace, size_t workspace_bytes,
+                      int32_t* status_dev, void* stream) {
+  if (q_len < 1 || heads < 1 || int64_t(heads) * q_len > 0x7fffffff) return QMLA_ERR_INVALID_ARG;
+  return decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
+                     max_seq_len, batch, heads * q_len, q_len, heads, q_c, q_r, softmax_scale,
+                     out, lse, workspace, workspace_bytes, status_dev, stream);
 }
 
 int qmla_read_status(const int32_t* status_dev, void* stream) {

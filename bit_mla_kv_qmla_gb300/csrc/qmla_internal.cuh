@@ -120,6 +120,12 @@ struct DecodeArgs {
   // blocks at the start of every non-empty sequence, so a worker whose range
   // crosses into another sequence gets that much less context.
   int piece_cost = 0;
+  // Multi-token query decode: heads = q_len * q_heads virtual heads, virtual
+  // head v being head v % q_heads of query v / q_heads; query i sits at
+  // position L - q_len + i and attends only to tokens up to it.  q_heads = 0:
+  // one query per sequence, every cached token visible.
+  int q_len = 1;
+  int q_heads = 0;
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (the

@@ -202,6 +202,28 @@ int qmla_decode(int format, const void* blocks, int64_t num_blocks,
                 void* workspace, size_t workspace_bytes,
                 int32_t* status_dev, void* stream);
 
+/* qmla_decode_multi - decode of q_len query tokens per sequence (a
+ * multi-token prediction or speculative-verification step), the last q_len
+ * tokens of each cached sequence: query i sits at position L - q_len + i and
+ * attends causally, to cached tokens 0 .. L - q_len + i (none when that is
+ * negative: O = 0, LSE = -inf).  The pages describe single-token decode only;
+ * this is the same attention over the same cache with a causal mask.
+ *   q_c   [batch][q_len][heads][512], q_r [batch][q_len][heads][64] bfloat16
+ *   out   [batch][q_len][heads][512] bfloat16, lse [batch][q_len][heads]
+ *   workspace  >= qmla_decode_workspace_bytes(format, batch, heads * q_len, ...)
+ * The kernels see heads * q_len query rows: 128 run on the tensor cores,
+ * other multiples of 16 up to 256 (16 included) on the CUDA cores.  Errors: as
+ * qmla_decode; INVALID_ARG for q_len < 1 or heads < 1; UNSUPPORTED when
+ * heads * q_len is not served. */
+int qmla_decode_multi(int format, const void* blocks, int64_t num_blocks,
+                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                      const int32_t* seq_lens, int32_t max_seq_len,
+                      int32_t batch, int32_t heads, int32_t q_len,
+                      const void* q_c, const void* q_r, float softmax_scale,
+                      void* out, float* lse,
+                      void* workspace, size_t workspace_bytes,
+                      int32_t* status_dev, void* stream);
+
 /* Size of the library's own decode scratch used by qmla_decode_noalloc. */
 #define QMLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB per device */
 

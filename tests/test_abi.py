@@ -30,7 +30,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["qmla_block_bytes", "qmla_append", "qmla_append_advance",
-                            "qmla_decode_workspace_bytes",
+                            "qmla_decode_workspace_bytes", "qmla_decode_multi",
                             "qmla_decode", "qmla_decode_noalloc", "qmla_read_status",
                             "qmla_error_string"])
 
@@ -99,6 +99,19 @@ def test_decode_rejects_bad_arguments(lib):
     assert call(qc=p + 8) == -1      # queries must be 16-byte aligned
     assert call(ws=p + 128) == -1    # workspace must be 256-byte aligned
     assert call(maxb=0) == -1
+    assert call(batch=0) == 0
+
+
+def test_decode_multi_rejects_bad_arguments(lib):
+    keep, p = _fake(4096)
+
+    def call(heads=16, q_len=2, batch=1, fmt=0):
+        return lib.qmla_decode_multi(fmt, p, 4, p, 4, p, 256, batch, heads, q_len, p, p,
+                                     ctypes.c_float(0.1), p, p, p, 1 << 20, p, None)
+    assert call(q_len=0) == -1
+    assert call(heads=0) == -1
+    assert call(heads=64, q_len=5) == -2   # 320 query rows: not served
+    assert call(heads=17, q_len=1) == -2
     assert call(batch=0) == 0
 
 

@@ -178,3 +178,27 @@ def test_decode_bad_block_and_length_are_flagged():
     torch.cuda.synchronize()
     assert cache.status.item() & QMLA_STATUS_BAD_LEN
     assert torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("fmt,heads,q_len", [("C4R4", 16, 8), ("C2R4", 16, 8), ("BF16", 16, 8),
+                                             ("C4R4", 64, 2), ("C4R4", 8, 2), ("C4R4", 16, 2)])
+def test_decode_multi_query(fmt, heads, q_len):
+    """Multi-token query decode (q_len queries per sequence, causal) against the
+    oracle, every row: 16 x 8 and 64 x 2 query rows run on the 128-head
+    tensor-core kernel, 8 x 2 and 16 x 2 on the CUDA cores.
+    Sequences shorter than q_len leave their first queries nothing to attend."""
+    w = W.Workload(f"multi_{fmt}_{heads}_{q_len}", fmt, 5, heads, 1000, 0, "lognormal8", 0, 37)
+    lens = [1, q_len + 1, 63, 130, 1000]
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cpu")
+    g = torch.Generator().manual_seed(41)
+    qc = torch.randn(5, q_len, heads, 512, generator=g).to(torch.bfloat16)
+    qr = torch.randn(5, q_len, heads, 64, generator=g).to(torch.bfloat16)
+    out, lse = Decoder(cache, heads, max(lens), q_len=q_len)(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    table = cache.block_table.cpu().numpy()
+    for b, L in enumerate(lens):
+        pool = oracle_pool_for_seq(w, b, L, table[b], cache.num_blocks, "cpu")
+        ro, rl = oracle.decode_multi(W.FORMATS[fmt], pool, table[b:b + 1], np.array([L]),
+                                     qc[b:b + 1], qr[b:b + 1], w.scale)
+        compare_rows(out[b], lse[b], ro[0], rl[0], f"{fmt} {heads}x{q_len} seq {b}")
