@@ -393,7 +393,48 @@ def measure_also(args, device):
         del cache, dec, flush
         torch.cuda.empty_cache()
     out.update(measure_multi(device, pk))
+    out.update(measure_fold(device))
     return out
+
+
+def measure_fold(device):
+    """Error of the low-bit decode with and without an orthogonal transform
+    folded into the content latent and query (c R, q_c R; the output rotated
+    back), on 8 x 2048-token sequences whose latents have 1% of the channels
+    at 10x gain.  Reference: the BF16-cache decode of the unrotated tokens.
+    Reported: mean |dLSE| and RMS output error relative to the reference's
+    RMS, for C4R4 and C2R4."""
+    import torch
+    from bit_mla_kv_qmla_gb300 import workloads as W
+    from bit_mla_kv_qmla_gb300.cache import Decoder, PagedCache
+    R = W.orthogonal(512, 3).to(device)
+    res = {}
+    ref = None
+    for fmt in ("BF16", "C4R4", "C2R4"):
+        w = W.Workload(f"fold_{fmt}", fmt, 8, 16, 2048, 0, "x10pct1", 0, 5)
+        lens = W.seq_lens(w)
+        table, nblocks = W.block_table(w, lens)
+        qc, qr = W.queries(w, device=device)
+        row = {}
+        for rot in ((False,) if fmt == "BF16" else (False, True)):
+            cache = PagedCache(fmt, table, nblocks, device)
+            for b, L in enumerate(lens):
+                lat, rope = W.tokens(w, b, L, device=device)
+                cache.append_seq(b, W.rotate(lat, R) if rot else lat, rope)
+            out, lse = Decoder(cache, 16, max(lens))(W.rotate(qc, R) if rot else qc, qr, w.scale)
+            o = out.double() @ R.T if rot else out.double()
+            if fmt == "BF16":
+                ref = (o, lse.double())
+                continue
+            rms = torch.sqrt(((o - ref[0]) ** 2).mean() / (ref[0] ** 2).mean()).item()
+            dl = (lse.double() - ref[1]).abs().mean().item()
+            row["rotated" if rot else "plain"] = {"mean_abs_dlse": round(dl, 5),
+                                                  "rel_rms_dO": round(rms, 5)}
+            del cache
+        if row:
+            res[fmt] = row
+    torch.cuda.empty_cache()
+    return {"folded_rotation_error_b8_h16_l2048_x10pct1": res}
 
 
 def measure_multi(device, pk):

@@ -155,3 +155,25 @@ def exact_grid_group(gen: torch.Generator, bits: int, n: int = 64,
     codes[perm[1]] = levels
     vals = codes.to(torch.float32) * scale + zero
     return vals, codes, zero
+
+
+def orthogonal(n: int, seed: int) -> torch.Tensor:
+    """Seeded random orthogonal matrix [n][n] in float64 (Haar-distributed: Q
+    of the QR factorization of a standard Gaussian matrix, with the column
+    signs that make diag(R) positive).
+
+    Stands in for a transform folded into the weights offline ("QuantMLA:
+    INT4 (and INT2) for both halves of the MLA cache", section "Key
+    findings"): folding R into the latent's down-projection and into the
+    absorbed query projection turns the cached latent c into c R and the
+    query q_c into q_c R, which leaves every exact score q_c . c unchanged
+    and the output O = P C into O R."""
+    g = _gen(seed * 1000003 + 61)
+    a = torch.randn(n, n, generator=g, dtype=torch.float64)
+    q, r = torch.linalg.qr(a)
+    return q * torch.sign(torch.diagonal(r)).unsqueeze(0)
+
+
+def rotate(x: torch.Tensor, R: torch.Tensor) -> torch.Tensor:
+    """x [...][n] (bfloat16) times R [n][n], rounded to bfloat16."""
+    return (x.to(torch.float64) @ R.to(x.device)).to(torch.bfloat16)

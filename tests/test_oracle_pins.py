@@ -554,3 +554,43 @@ def test_decode_multi_matches_explicit_causal_mask():
             assert np.allclose(lse[b, i], logsumexp(S, axis=1), rtol=0, atol=1e-12)
             ref = softmax(S, axis=1) @ lat[b, :L].double().numpy()
             assert np.allclose(O[b, i], ref, rtol=0, atol=1e-12)
+
+
+def _fold_case(fmt, R, lens, w):
+    """Oracle decode of workload w's tokens, rotated by R when R is given
+    (content latent and content query: c R, q_c R; the output rotated back)."""
+    Lm = max(lens)
+    lat = torch.stack([W.tokens(w, b, Lm)[0] for b in range(len(lens))])
+    rope = torch.stack([W.tokens(w, b, Lm)[1] for b in range(len(lens))])
+    qc, qr = W.queries(w)
+    if R is not None:
+        lat, qc = W.rotate(lat, R), W.rotate(qc, R)
+    blocks, table = _build_cache(fmt, lat, rope, lens)
+    O, lse = oracle.decode(fmt, blocks, table, np.array(lens), qc, qr, w.scale)
+    if R is not None:
+        O = O @ R.numpy().T
+    return O, lse
+
+
+def test_folded_rotation_keeps_scores_and_shrinks_quantization_error():
+    """The transform-folding mechanism ("QuantMLA: INT4 (and INT2) for both
+    halves of the MLA cache", Key findings): an orthogonal R folded into the
+    content latent and query leaves the exact attention unchanged (up to the
+    bfloat16 rounding of the rotated inputs) and, on latents with outlier
+    channels, shrinks the INT2 content cache's error, because it spreads
+    each outlier over every 64-channel group."""
+    w = W.Workload("fold_x10", "C2R4", 3, 4, 300, 0, "x10pct1", 0, 5)
+    R = W.orthogonal(512, 3)
+    lens = [300, 257, 64]
+    O0, l0 = _fold_case(oracle.BF16, None, lens, w)
+    O1, l1 = _fold_case(oracle.BF16, R, lens, w)
+    assert np.abs(l1 - l0).max() < 0.05
+    assert np.abs(O1 - O0).max() / np.abs(O0).max() < 0.05
+    rms = lambda O: np.sqrt(((O - O0) ** 2).mean() / (O0 ** 2).mean())
+    for fmt in (oracle.C4R4, oracle.C2R4):
+        Op, lp = _fold_case(fmt, None, lens, w)
+        Or, lr = _fold_case(fmt, R, lens, w)
+        # mean |dLSE| and relative RMS output error against the exact decode
+        lse_plain, lse_rot = np.abs(lp - l0).mean(), np.abs(lr - l0).mean()
+        assert lse_rot < 0.6 * lse_plain, (fmt, lse_plain, lse_rot)
+        assert rms(Or) < 0.75 * rms(Op), (fmt, rms(Op), rms(Or))
