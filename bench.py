@@ -347,7 +347,9 @@ def run_ours(args, rank, world, device):
     roof = roofline_for(w.fmt, w.heads, lens_mid, t_dec, pk, recorded_traffic(w.name))
     roof["decode_ms"] = round(t_dec * 1e3, 5)
     tc = w.heads in (16, 128) and w.fmt in ("C4R4", "C2R4")
-    roof["kernel"] = (f"decode_tc{w.heads} (tcgen05) + plan + combine" if tc else
+    roof["kernel"] = ((f"decode_tc{w.heads} (tcgen05"
+                       + (", plans its own pieces)" if w.heads == 16 and w.batch <= 64
+                          else ") + plan") + " + combine") if tc else
                       "decode_simt (CUDA cores) + combine") + ", CUDA events per qmla_decode call"
     res = {"tokens": tokens, "elapsed": elapsed, "t_dec": t_dec, "roofline": roof,
            "dtype": "f16" if tc else "f32",
