@@ -245,3 +245,38 @@ def test_decode_folded_rotation(fmt):
     rms = {k: np.sqrt(((v[0] - O0) ** 2).mean() / (O0 ** 2).mean()) for k, v in results.items()}
     dl = {k: np.abs(v[1] - l0).mean() for k, v in results.items()}
     assert dl[True] < 0.6 * dl[False] and rms[True] < 0.75 * rms[False], (dl, rms)
+
+
+@pytest.mark.parametrize("batch", [64, 65])
+def test_decode_plan_source_boundary(batch):
+    """64 sequences: the 16-head kernel plans its own pieces; 65: the planner
+    kernel does.  Same tokens, same results within the tolerance."""
+    w = W.Workload(f"bound_{batch}", "C4R4", batch, 16, 200, 0, "lognormal8", 0, 43)
+    rng = np.random.default_rng(batch)
+    lens = [int(x) for x in rng.integers(0, 200, batch)]
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cpu")
+    qc, qr = W.queries(w)
+    out, lse = Decoder(cache, 16, max(lens))(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    table = cache.block_table.cpu().numpy()
+    for b in (0, 31, batch - 1):
+        L = lens[b]
+        pool = oracle_pool_for_seq(w, b, L, table[b], cache.num_blocks, "cpu")
+        o, l = oracle.decode(W.FORMATS[w.fmt], pool, table[b:b + 1], np.array([L]),
+                             qc[b:b + 1].cpu(), qr[b:b + 1].cpu(), w.scale)
+        compare_rows(out[b:b + 1], lse[b:b + 1], o, l, f"batch {batch} seq {b}")
+
+
+def test_decode_max_heads():
+    """256 query heads, the most any kernel serves (the CUDA-core kernel)."""
+    w = W.Workload("heads256", "C4R4", 2, 256, 300, 0, "lognormal8", 0, 47)
+    lens = [300, 65]
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cpu")
+    qc, qr = W.queries(w)
+    out, lse = Decoder(cache, 256, max(lens))(qc.cuda(), qr.cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    ref_o, ref_l = _oracle_full(w, cache, lens, qc, qr, "cpu")
+    hs = sample_heads(256, 24, 5)
+    compare_rows(out[:, hs], lse[:, hs], ref_o[:, hs], ref_l[:, hs], "H256")
