@@ -115,9 +115,6 @@ __device__ __forceinline__ void ld_nc_v4(const void* p, uint32_t* r) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "l"(p));
 }
-__device__ __forceinline__ void ld_nc_v2(const void* p, uint32_t& a, uint32_t& b) {
-  asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
-}
 __device__ __forceinline__ uint32_t ld_nc_b32(const void* p) {
   uint32_t a;
   asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(a) : "l"(p));
