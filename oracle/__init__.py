@@ -29,7 +29,9 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-C4R4, C2R4, BF16 = 0, 1, 2
+C4R4, C2R4, BF16, C4R2, C2R2 = 0, 1, 2, 3, 4
+CONTENT_BITS = {C4R4: 4, C2R4: 2, C4R2: 4, C2R2: 2}
+ROPE_BITS = {C4R4: 4, C2R4: 4, C4R2: 2, C2R2: 2}
 RN, RD, RU = 0, 1, 2
 D_C, D_R, GROUP, SLOTS = 512, 64, 64, 64
 

@@ -12,6 +12,11 @@
 //    mermaid flowchart): each token stores a content latent and a decoupled
 //    RoPE key; content is quantized to INT4 or INT2, the RoPE key to INT4;
 //    dequantization happens inside attention.
+//  * Same page, "Key findings": generic quantizers treat the content latent
+//    and the RoPE key as one tensor with one bit width.  The formats C4R2
+//    and C2R2 (RoPE key at INT2, the same 64-channel groups and grid) are
+//    that comparison: the RoPE codes shrink from 16 to 8 bytes per token and
+//    block half, everything else keeps its place.
 //  * Same page, "Key findings": the learned transforms are folded into the
 //    weights offline, so inputs here are already transformed.
 //  * Parameters the pages leave open, fixed by this library: 64-channel
@@ -40,7 +45,7 @@ constexpr int kDr = 64;    // RoPE key channels
 constexpr int kGroup = 64; // channels per quantization group
 constexpr int kSlots = 64; // token slots per block
 
-enum Format { C4R4 = 0, C2R4 = 1, BF16 = 2 };
+enum Format { C4R4 = 0, C2R4 = 1, BF16 = 2, C4R2 = 3, C2R2 = 4 };
 enum Round { RN = 0, RD = 1, RU = 2 };
 
 float from_bits(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
@@ -247,11 +252,14 @@ void unpack_codes(const uint8_t* in, int nch, int bits, uint8_t* codes) {
   }
 }
 
-int content_bits(int fmt) { return fmt == C4R4 ? 4 : 2; }
+int content_bits(int fmt) { return (fmt == C4R4 || fmt == C4R2) ? 4 : 2; }
+int rope_bits(int fmt) { return (fmt == C4R2 || fmt == C2R2) ? 2 : 4; }
 size_t code_bytes_per_group(int fmt) { return size_t(kGroup * content_bits(fmt) / 8); }
+// RoPE code bytes of one token in one block half (32 channels)
+size_t rope_code_bytes(int fmt) { return size_t(32 * rope_bits(fmt) / 8); }
 size_t half_bytes(int fmt) {
   if (fmt == BF16) return size_t(4 * kSlots * kGroup * 2 + kSlots * 32 * 2);
-  return 4 * kSlots * code_bytes_per_group(fmt) + kSlots * 16 + 4 * kSlots * 4;
+  return 4 * kSlots * code_bytes_per_group(fmt) + kSlots * rope_code_bytes(fmt) + 4 * kSlots * 4;
 }
 size_t block_bytes(int fmt) {
   if (fmt == BF16) return 2 * half_bytes(fmt);
@@ -264,12 +272,13 @@ size_t off_content_codes(int fmt, int g, int slot) {
   return h * half_bytes(fmt) + (size_t(gi) * kSlots + slot) * code_bytes_per_group(fmt);
 }
 size_t off_rope_codes(int fmt, int h, int slot) {
-  return h * half_bytes(fmt) + 4 * kSlots * code_bytes_per_group(fmt) + size_t(slot) * 16;
+  return h * half_bytes(fmt) + 4 * kSlots * code_bytes_per_group(fmt) +
+         size_t(slot) * rope_code_bytes(fmt);
 }
 size_t off_content_sz(int fmt, int g, int slot) {
   const int h = g / 4, gi = g % 4;
-  return h * half_bytes(fmt) + 4 * kSlots * code_bytes_per_group(fmt) + kSlots * 16 +
-         (size_t(gi) * kSlots + slot) * 4;
+  return h * half_bytes(fmt) + 4 * kSlots * code_bytes_per_group(fmt) +
+         kSlots * rope_code_bytes(fmt) + (size_t(gi) * kSlots + slot) * 4;
 }
 size_t off_rope_sz(int fmt, int slot) { return 2 * half_bytes(fmt) + size_t(slot) * 4; }
 size_t off_bf16_content(int g, int slot) {
@@ -301,10 +310,12 @@ void write_token(int fmt, uint8_t* blk, int slot, const uint16_t* lat, const uin
     put_u16(blk + off_content_sz(fmt, g, slot), s);
     put_u16(blk + off_content_sz(fmt, g, slot) + 2, z);
   }
+  // the RoPE key: one 64-channel group; channels 0-31 go to half 0, 32-63 to half 1
+  const int rb = rope_bits(fmt);
   for (int i = 0; i < kDr; ++i) x[i] = bf16_to_f32(rope[i]);
-  quantize_group(x, kDr, 4, &s, &z, codes);
-  pack_codes(codes, 32, 4, blk + off_rope_codes(fmt, 0, slot));
-  pack_codes(codes + 32, 32, 4, blk + off_rope_codes(fmt, 1, slot));
+  quantize_group(x, kDr, rb, &s, &z, codes);
+  pack_codes(codes, 32, rb, blk + off_rope_codes(fmt, 0, slot));
+  pack_codes(codes + 32, 32, rb, blk + off_rope_codes(fmt, 1, slot));
   put_u16(blk + off_rope_sz(fmt, slot), s);
   put_u16(blk + off_rope_sz(fmt, slot) + 2, z);
 }
@@ -328,8 +339,9 @@ void read_token(int fmt, const uint8_t* blk, int slot, float* out576) {
       out576[g * kGroup + i] = prod + z;
     }
   }
-  unpack_codes(blk + off_rope_codes(fmt, 0, slot), 32, 4, codes);
-  unpack_codes(blk + off_rope_codes(fmt, 1, slot), 32, 4, codes + 32);
+  const int rb = rope_bits(fmt);
+  unpack_codes(blk + off_rope_codes(fmt, 0, slot), 32, rb, codes);
+  unpack_codes(blk + off_rope_codes(fmt, 1, slot), 32, rb, codes + 32);
   const float s = f16_to_f32(get_u16(blk + off_rope_sz(fmt, slot)));
   const float z = f16_to_f32(get_u16(blk + off_rope_sz(fmt, slot) + 2));
   for (int j = 0; j < kDr; ++j) {
@@ -395,7 +407,7 @@ void oracle_grid_for(float mn, float mx, int levels, int* E, double* Z, double* 
 }
 
 size_t oracle_block_bytes(int fmt) {
-  if (fmt < 0 || fmt > 2) return 0;
+  if (fmt < 0 || fmt > 4) return 0;
   return block_bytes(fmt);
 }
 

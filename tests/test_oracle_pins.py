@@ -256,13 +256,16 @@ def test_pack_unpack_roundtrip(bits):
 
 def test_block_bytes_formula():
     # bytes/token = d_c*b_c/8 + d_r*b_r/8 + 4*(d_c/G + d_r/G)  (fp16 scale + zero per group)
-    for fmt, bc in [(oracle.C4R4, 4), (oracle.C2R4, 2)]:
-        per_tok = 512 * bc // 8 + 64 * 4 // 8 + 4 * (512 // 64 + 64 // 64)
+    for fmt, bc, br in [(oracle.C4R4, 4, 4), (oracle.C2R4, 2, 4), (oracle.C4R2, 4, 2),
+                        (oracle.C2R2, 2, 2)]:
+        per_tok = 512 * bc // 8 + 64 * br // 8 + 4 * (512 // 64 + 64 // 64)
         assert oracle.block_bytes(fmt) == 64 * per_tok
     assert oracle.block_bytes(oracle.BF16) == 64 * 576 * 2
     assert (oracle.block_bytes(oracle.C4R4), oracle.block_bytes(oracle.C2R4)) == (20736, 12544)
+    assert (oracle.block_bytes(oracle.C4R2), oracle.block_bytes(oracle.C2R2)) == (19712, 11520)
     ratio = oracle.block_bytes(oracle.BF16) / oracle.block_bytes(oracle.C4R4)
     assert abs(ratio - 3.5556) < 1e-3  # the pages report 3.59x for their own layout
+    assert oracle.block_bytes(5) == 0 and oracle.block_bytes(-1) == 0
 
 
 def _one_token(seed):
@@ -272,8 +275,15 @@ def _one_token(seed):
     return lat, rope
 
 
-@pytest.mark.parametrize("fmt,cb,half", [(oracle.C4R4, 32, 10240), (oracle.C2R4, 16, 6144)])
-def test_layout_offsets_match_spec(fmt, cb, half):
+# (format, content code bytes per group, RoPE code bytes per half, half bytes):
+# a half is 4 content groups x 64 tokens, then 64 tokens of RoPE codes, then
+# 4 x 64 content scale/zero words
+_LAYOUTS = [(oracle.C4R4, 32, 16, 10240), (oracle.C2R4, 16, 16, 6144),
+            (oracle.C4R2, 32, 8, 9728), (oracle.C2R2, 16, 8, 5632)]
+
+
+@pytest.mark.parametrize("fmt,cb,rb,half", _LAYOUTS)
+def test_layout_offsets_match_spec(fmt, cb, rb, half):
     """A token written to slot 5 touches exactly the byte ranges the layout
     specification assigns to slot 5, and those ranges hold the quantizer's
     output for the right group."""
@@ -284,25 +294,49 @@ def test_layout_offsets_match_spec(fmt, cb, half):
     touched = np.zeros_like(blocks, dtype=bool)
     xl = lat.float().numpy()[0, 0]
     xr = rope.float().numpy()[0, 0]
-    bits = 4 if fmt == oracle.C4R4 else 2
+    bits, rbits = cb // 8, rb // 4
+    assert half == 4 * 64 * cb + 64 * rb + 1024
     for grp in range(8):
         h, gi = divmod(grp, 4)
         c0 = h * half + (gi * 64 + slot) * cb
-        sz0 = h * half + 4 * 64 * cb + 1024 + (gi * 64 + slot) * 4
+        sz0 = h * half + 4 * 64 * cb + 64 * rb + (gi * 64 + slot) * 4
         touched[c0:c0 + cb] = True
         touched[sz0:sz0 + 4] = True
         sb, zb, codes = oracle.quantize_group(xl[grp * 64:(grp + 1) * 64], bits)
         assert np.array_equal(blocks[c0:c0 + cb], oracle.pack_codes(codes, bits))
         assert blocks[sz0:sz0 + 4].view(np.uint16).tolist() == [sb, zb]
-    sb, zb, codes = oracle.quantize_group(xr, 4)
+    sb, zb, codes = oracle.quantize_group(xr, rbits)
     for h in range(2):
-        r0 = h * half + 4 * 64 * cb + slot * 16
-        touched[r0:r0 + 16] = True
-        assert np.array_equal(blocks[r0:r0 + 16], oracle.pack_codes(codes[32 * h:32 * h + 32], 4))
+        r0 = h * half + 4 * 64 * cb + slot * rb
+        touched[r0:r0 + rb] = True
+        assert np.array_equal(blocks[r0:r0 + rb],
+                              oracle.pack_codes(codes[32 * h:32 * h + 32], rbits))
     rs = 2 * half + slot * 4
     touched[rs:rs + 4] = True
     assert blocks[rs:rs + 4].view(np.uint16).tolist() == [sb, zb]
     assert not np.any(blocks[~touched])
+
+
+@pytest.mark.parametrize("fmt_r4,fmt_r2", [(oracle.C4R4, oracle.C4R2), (oracle.C2R4, oracle.C2R2)])
+def test_rope_int2_changes_only_the_rope_key(fmt_r4, fmt_r2):
+    """The RoPE-at-INT2 formats dequantize the content latent exactly as their
+    RoPE-INT4 counterparts do; the RoPE key stays within the 2-bit bound
+    |x - x_hat| <= s/2 (+ rounding) of its own group."""
+    lat, rope = _one_token(11)
+    out = {}
+    for fmt in (fmt_r4, fmt_r2):
+        blocks = np.zeros(oracle.block_bytes(fmt), np.uint8)
+        oracle.append(fmt, blocks, np.zeros((1, 1), np.int32), np.array([3], np.int32), lat, rope)
+        out[fmt] = oracle.read_token(fmt, blocks, 3)
+    assert np.array_equal(out[fmt_r4][:512], out[fmt_r2][:512])
+    xr = rope.float().numpy()[0, 0]
+    sb, zb, codes = oracle.quantize_group(xr, 2)
+    assert codes.max() <= 3
+    s = float(np.array([sb], np.uint16).view(np.float16)[0])
+    err2 = np.abs(out[fmt_r2][512:] - xr)
+    err4 = np.abs(out[fmt_r4][512:] - xr)
+    assert np.all(err2 <= s / 2 + 1e-6 * (1 + np.abs(xr)))
+    assert err2.max() > err4.max()
 
 
 def test_layout_offsets_bf16():
@@ -368,7 +402,7 @@ def test_decode_bf16_matches_library_softmax():
         assert np.allclose(O[b], ref, rtol=0, atol=1e-12)
 
 
-def _grid_tokens(B, L, bits_c, seed):
+def _grid_tokens(B, L, bits_c, seed, bits_r=4):
     g = torch.Generator().manual_seed(seed)
     lat = torch.empty(B, L, 512)
     rope = torch.empty(B, L, 64)
@@ -376,14 +410,15 @@ def _grid_tokens(B, L, bits_c, seed):
         for t in range(L):
             for grp in range(8):
                 lat[b, t, grp * 64:(grp + 1) * 64] = W.exact_grid_group(g, bits_c)[0]
-            rope[b, t] = W.exact_grid_group(g, 4)[0]
+            rope[b, t] = W.exact_grid_group(g, bits_r)[0]
     return lat.to(torch.bfloat16), rope.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("fmt,bits", [(oracle.C4R4, 4), (oracle.C2R4, 2)])
-def test_quantized_decode_equals_bf16_on_exact_grid(fmt, bits):
+@pytest.mark.parametrize("fmt", [oracle.C4R4, oracle.C2R4, oracle.C4R2, oracle.C2R2])
+def test_quantized_decode_equals_bf16_on_exact_grid(fmt):
+    bits, rbits = oracle.CONTENT_BITS[fmt], oracle.ROPE_BITS[fmt]
     B, H, lens = 2, 3, [70, 5]
-    lat, rope = _grid_tokens(B, 70, bits, 50 + bits)
+    lat, rope = _grid_tokens(B, 70, bits, 50 + bits + (7 if rbits == 2 else 0), rbits)
     qc, qr = _rand((B, H, 512), 5), _rand((B, H, 64), 6)
     bq, tq = _build_cache(fmt, lat, rope, lens)
     bb, tb = _build_cache(oracle.BF16, lat, rope, lens)
@@ -454,7 +489,7 @@ def test_decode_dominant_token():
     assert np.allclose(O[0, 0], x[t_star], atol=1e-9)
 
 
-@pytest.mark.parametrize("fmt", [oracle.C4R4, oracle.C2R4])
+@pytest.mark.parametrize("fmt", [oracle.C4R4, oracle.C2R4, oracle.C2R2])
 def test_split_merge_equals_unsplit(fmt):
     L = 64 * 7 + 13
     lat, rope = _rand((1, L, 512), 12), _rand((1, L, 64), 13)
@@ -480,7 +515,7 @@ def test_block_permutation_invariance():
     assert np.array_equal(O1, O2) and np.array_equal(l1, l2)
 
 
-@pytest.mark.parametrize("fmt", [oracle.C4R4, oracle.C2R4, oracle.BF16])
+@pytest.mark.parametrize("fmt", [oracle.C4R4, oracle.C2R4, oracle.BF16, oracle.C4R2])
 def test_incremental_append_equals_bulk(fmt):
     L = 100
     lat, rope = _rand((1, L, 512), 20), _rand((1, L, 64), 21)
