@@ -396,6 +396,7 @@ def measure_also(args, device):
         torch.cuda.empty_cache()
     out.update(measure_multi(device, pk))
     out.update(measure_fold(device))
+    out.update(measure_rope_bits(device))
     return out
 
 
@@ -437,6 +438,72 @@ def measure_fold(device):
             res[fmt] = row
     torch.cuda.empty_cache()
     return {"folded_rotation_error_b8_h16_l2048_x10pct1": res}
+
+
+def measure_rope_bits(device):
+    """The equal-bits comparison: the RoPE key at INT4 (C4R4, C2R4) against
+    INT2 (C4R2, C2R2), as a generic quantizer that gives both halves of the
+    cache one bit width would store it.  Synthetic latents with 1% of the
+    channels at 10x gain, N(0, 1) RoPE keys and queries, 16 heads.
+    * score error: 4096 one-token sequences, so that each LSE is exactly that
+      token's score (natural-log units, scale included); the content path
+      alone (q_r = 0), the RoPE path alone (q_c = 0) and both, as RMS of the
+      difference to the BF16-cache scores;
+    * decode error: 8 x 2048-token sequences, mean |dLSE| and the RMS output
+      error relative to the BF16-cache decode's RMS.
+    The INT2-RoPE formats run on the CUDA-core decode kernel."""
+    import torch
+    from bit_mla_kv_qmla_gb300 import qmla_block_bytes
+    from bit_mla_kv_qmla_gb300 import workloads as W
+    from bit_mla_kv_qmla_gb300.cache import Decoder, PagedCache
+    fmts = ("BF16", "C4R4", "C4R2", "C2R4", "C2R2")
+    # scores: B one-token sequences
+    w1 = W.Workload("ropebits_l1", "BF16", 4096, 16, 1, 0, "x10pct1", 0, 6)
+    lat, rope = W.tokens(w1, 0, w1.batch, device=device)
+    qc, qr = W.queries(w1, device=device)
+    variants = {"both": (qc, qr), "content_path": (qc, torch.zeros_like(qr)),
+                "rope_path": (torch.zeros_like(qc), qr)}
+    table, nblocks = W.block_table(w1, [1] * w1.batch)
+    scores = {}
+    for fmt in fmts:
+        cache = PagedCache(fmt, table, nblocks, device)
+        cache.append(lat[:, None].contiguous(), rope[:, None].contiguous())
+        dec = Decoder(cache, 16, 1)
+        scores[fmt] = {k: dec(a, b, w1.scale)[1].double().clone() for k, (a, b) in variants.items()}
+        assert int(cache.status.item()) == 0
+        del cache, dec
+    score_err = {}
+    for fmt in fmts[1:]:
+        score_err[fmt] = {k: round(torch.sqrt(((scores[fmt][k] - scores["BF16"][k]) ** 2)
+                                              .mean()).item(), 5) for k in variants}
+    score_rms = {k: round(torch.sqrt((scores["BF16"][k] ** 2).mean()).item(), 4)
+                 for k in variants}
+    # attention outputs
+    dec_err, ref = {}, None
+    for fmt in fmts:
+        w = W.Workload(f"ropebits_{fmt}", fmt, 8, 16, 2048, 0, "x10pct1", 0, 5)
+        lens = W.seq_lens(w)
+        t2, nb2 = W.block_table(w, lens)
+        q2c, q2r = W.queries(w, device=device)
+        cache = PagedCache(fmt, t2, nb2, device)
+        for b, L in enumerate(lens):
+            cache.append_seq(b, *W.tokens(w, b, L, device=device))
+        out, lse = Decoder(cache, 16, max(lens))(q2c, q2r, w.scale)
+        o, l = out.double(), lse.double()
+        if fmt == "BF16":
+            ref = (o, l)
+        else:
+            dec_err[fmt] = {
+                "mean_abs_dlse": round((l - ref[1]).abs().mean().item(), 5),
+                "rel_rms_dO": round(torch.sqrt(((o - ref[0]) ** 2).mean()
+                                               / (ref[0] ** 2).mean()).item(), 5)}
+        del cache
+    torch.cuda.empty_cache()
+    return {"rope_bits_ablation_h16_x10pct1": {
+        "bytes_per_token": {f: qmla_block_bytes(f) // 64 for f in fmts},
+        "score_rms_bf16_l1_b4096": score_rms,
+        "score_rms_error_l1_b4096": score_err,
+        "decode_error_b8_l2048": dec_err}}
 
 
 def measure_multi(device, pk):

@@ -11,8 +11,8 @@ from typing import Optional
 
 from . import _lib
 
-C4R4, C2R4, BF16 = 0, 1, 2
-FORMAT_NAMES = {"C4R4": C4R4, "C2R4": C2R4, "BF16": BF16}
+C4R4, C2R4, BF16, C4R2, C2R2 = 0, 1, 2, 3, 4
+FORMAT_NAMES = {"C4R4": C4R4, "C2R4": C2R4, "BF16": BF16, "C4R2": C4R2, "C2R2": C2R2}
 D_C, D_R, GROUP, BLOCK_TOKENS = 512, 64, 64, 64
 
 QMLA_OK = 0

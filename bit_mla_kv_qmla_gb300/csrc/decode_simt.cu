@@ -70,10 +70,13 @@ __device__ __forceinline__ void dequant8(const Geom& G, const uint8_t* blk, int 
     first = ch % per_word;
     sz = *reinterpret_cast<const uint32_t*>(half + G.sz_off + (gi * kT + slot) * 4);
   } else {
-    const int r = seg - 64;  // RoPE channels 8r .. 8r+7
-    bits = 4;
-    word = reinterpret_cast<const uint32_t*>(blk + (r / 4) * G.half + G.rope_off + slot * 16)[r % 4];
-    first = 0;
+    const int r = seg - 64;  // RoPE channels 8r .. 8r+7, block half r / 4
+    bits = G.rbits;
+    const int ch = (r % 4) * 8;  // channel inside the half's 32
+    const int per_word = 32 / bits;
+    word = reinterpret_cast<const uint32_t*>(blk + (r / 4) * G.half + G.rope_off +
+                                             slot * G.rope_bytes)[ch / per_word];
+    first = ch % per_word;
     sz = *reinterpret_cast<const uint32_t*>(blk + G.rope_sz_off + slot * 4);
   }
   const float s = __half2float(__ushort_as_half(uint16_t(sz & 0xffff)));

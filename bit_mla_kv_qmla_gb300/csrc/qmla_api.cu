@@ -11,7 +11,9 @@
 namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-bool known_format(int f) { return f == QMLA_C4R4 || f == QMLA_C2R4 || f == QMLA_BF16; }
+bool known_format(int f) {
+  return f == QMLA_C4R4 || f == QMLA_C2R4 || f == QMLA_BF16 || f == QMLA_C4R2 || f == QMLA_C2R2;
+}
 
 int device_sms() {
   int dev = 0, sms = 0;

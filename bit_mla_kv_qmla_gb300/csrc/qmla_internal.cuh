@@ -28,12 +28,16 @@ struct Geom {
   int sz_off;       // offset of content scale/zero inside a half
   int rope_sz_off;  // offset of the shared RoPE scale/zero inside the block
   int block;        // bytes of a block
+  int rbits;        // RoPE code bits (4, 2; 16 = bf16)
+  int rope_bytes;   // bytes of one token's 32 RoPE channels in a half (16, 8, 64)
 };
 
 __host__ __device__ constexpr Geom geom(int fmt) {
-  return fmt == QMLA_C4R4 ? Geom{QMLA_C4R4, 4, 32, 10240, 0, 8192, 9216, 20480, 20736}
-       : fmt == QMLA_C2R4 ? Geom{QMLA_C2R4, 2, 16, 6144, 0, 4096, 5120, 12288, 12544}
-                          : Geom{QMLA_BF16, 16, 128, 36864, 0, 32768, -1, -1, 73728};
+  return fmt == QMLA_C4R4 ? Geom{QMLA_C4R4, 4, 32, 10240, 0, 8192, 9216, 20480, 20736, 4, 16}
+       : fmt == QMLA_C2R4 ? Geom{QMLA_C2R4, 2, 16, 6144, 0, 4096, 5120, 12288, 12544, 4, 16}
+       : fmt == QMLA_C4R2 ? Geom{QMLA_C4R2, 4, 32, 9728, 0, 8192, 8704, 19456, 19712, 2, 8}
+       : fmt == QMLA_C2R2 ? Geom{QMLA_C2R2, 2, 16, 5632, 0, 4096, 4608, 11264, 11520, 2, 8}
+                          : Geom{QMLA_BF16, 16, 128, 36864, 0, 32768, -1, -1, 73728, 16, 64};
 }
 
 // Device status word: OR in a bit (relaxed; read by the host after a sync).

@@ -102,8 +102,8 @@ __device__ __forceinline__ uint32_t pack_word(uint32_t c0, uint32_t c1, int bits
 }
 
 // One warp quantizes and stores group g of a token (g 0-7: content groups,
-// 8: the RoPE key) at slot `slot` of block `blk`; lane holds the group's
-// channels 2*lane and 2*lane+1 in v.
+// 8: the RoPE key, INT4 or INT2 by format) at slot `slot` of block `blk`;
+// lane holds the group's channels 2*lane and 2*lane+1 in v.
 __device__ __forceinline__ void store_group(int fmt, uint8_t* blk, int slot, int g,
                                             __nv_bfloat162 v, int lane) {
   const Geom G = geom(fmt);
@@ -120,7 +120,7 @@ __device__ __forceinline__ void store_group(int fmt, uint8_t* blk, int slot, int
     return;
   }
   const float x0 = __bfloat162float(v.x), x1 = __bfloat162float(v.y);
-  const int bits = (g < 8) ? G.cbits : 4;
+  const int bits = (g < 8) ? G.cbits : G.rbits;
   uint32_t c0, c1;
   uint16_t s_bits, z_bits;
   quantize_pair(x0, x1, bits, c0, c1, s_bits, z_bits);
@@ -135,10 +135,13 @@ __device__ __forceinline__ void store_group(int fmt, uint8_t* blk, int slot, int
       reinterpret_cast<uint32_t*>(half + G.content_off + (gi * kT + slot) * G.code_bytes)[w] = word;
     if (lane == 0) reinterpret_cast<uint32_t*>(half + G.sz_off + (gi * kT + slot) * 4)[0] = sz;
   } else {
-    // RoPE: 8 words of 8 channels; words 0-3 -> half 0, words 4-7 -> half 1
-    if (lane % 4 == 0) {
-      const int h = w / 4;
-      reinterpret_cast<uint32_t*>(blk + h * G.half + G.rope_off + slot * 16)[w % 4] = word;
+    // RoPE: 8 words of 8 channels (INT4) or 4 of 16 (INT2); the first half
+    // of the words (channels 0-31) goes to block half 0, the rest to half 1
+    if (lane % per_word_lanes == 0) {
+      const int words_per_half = bits;  // 32 channels / (32 / bits)
+      const int h = w / words_per_half;
+      reinterpret_cast<uint32_t*>(blk + h * G.half + G.rope_off + slot * G.rope_bytes)
+          [w % words_per_half] = word;
     }
     if (lane == 0) reinterpret_cast<uint32_t*>(blk + G.rope_sz_off + slot * 4)[0] = sz;
   }

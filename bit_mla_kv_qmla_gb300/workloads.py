@@ -35,13 +35,13 @@ from typing import List, Optional, Sequence
 import torch
 
 D_C, D_R, BLOCK = 512, 64, 64
-FORMATS = {"C4R4": 0, "C2R4": 1, "BF16": 2}
+FORMATS = {"C4R4": 0, "C2R4": 1, "BF16": 2, "C4R2": 3, "C2R2": 4}
 
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    fmt: str                # "C4R4" | "C2R4" | "BF16"
+    fmt: str                # "C4R4" | "C2R4" | "BF16" | "C4R2" | "C2R2"
     batch: int
     heads: int
     seq_len: int            # fixed length, or the upper bound when varlen

@@ -10,6 +10,10 @@
  *     part, d_r = 64 channels);
  *   - the content latent is stored at INT4 or INT2, the RoPE key at INT4
  *     ("C4R4" / "C2R4"), and the RoPE path is never taken below INT4;
+ *   - for the comparison with generic quantizers, which give both halves one
+ *     bit width ("Key findings" of the first page), the RoPE key can also be
+ *     stored at INT2 ("C4R2" / "C2R2"); these two formats are served by the
+ *     CUDA-core decode kernel only;
  *   - a native low-bit attention kernel unpacks and dequantizes inside the
  *     attention computation; nothing is expanded back to a 16-bit cache.
  * The learned path-specific transforms are folded into the model weights
@@ -51,15 +55,18 @@
  * Block layout (one block = 64 token slots; slot = position % 64).  A block is
  * split into two "halves": half h holds content channels 256h .. 256h+255
  * (content groups 4h .. 4h+3) and RoPE channels 32h .. 32h+31.
- *   C4R4 (CB = 32 code bytes per content group per token, HALF = 10240 B)
- *   C2R4 (CB = 16,                                        HALF =  6144 B)
+ *   C4R4 (CB = 32 code bytes per content group per token, RB = 16, HALF = 10240 B)
+ *   C2R4 (CB = 16,                                        RB = 16, HALF =  6144 B)
+ *   C4R2 (CB = 32,                                        RB =  8, HALF =  9728 B)
+ *   C2R2 (CB = 16,                                        RB =  8, HALF =  5632 B)
  *     half h at byte h*HALF:
  *       content codes   [4 groups][64 slots][CB]             (4*64*CB B)
- *       RoPE codes      [64 slots][16]  (32 channels, INT4)  (1024 B)
+ *       RoPE codes      [64 slots][RB] (32 channels, INT4 or INT2) (64*RB B)
  *       content s/z     [4 groups][64 slots][2] binary16 (scale, zero) (1024 B)
  *     RoPE s/z at byte 2*HALF: [64 slots][2] binary16 (scale, zero) (256 B);
  *     the RoPE key is one 64-channel group, so both halves share it.
- *     Block bytes: C4R4 20736 (324 B/token), C2R4 12544 (196 B/token).
+ *     Block bytes: C4R4 20736 (324 B/token), C2R4 12544 (196 B/token),
+ *     C4R2 19712 (308 B/token), C2R2 11520 (180 B/token).
  *   BF16 (comparison cache, no quantization, HALF = 36864 B)
  *     half h at byte h*HALF:
  *       content  [4 groups][64 slots][64] bfloat16   (32768 B)
@@ -107,7 +114,9 @@ extern "C" {
 typedef enum {
   QMLA_C4R4 = 0, /* content INT4, RoPE INT4 */
   QMLA_C2R4 = 1, /* content INT2, RoPE INT4 */
-  QMLA_BF16 = 2  /* unquantized bfloat16 comparison cache */
+  QMLA_BF16 = 2, /* unquantized bfloat16 comparison cache */
+  QMLA_C4R2 = 3, /* content INT4, RoPE INT2 (equal-bits comparison) */
+  QMLA_C2R2 = 4  /* content INT2, RoPE INT2 (equal-bits comparison) */
 } qmla_format;
 
 enum {
@@ -125,8 +134,8 @@ enum {
 #define QMLA_STATUS_BAD_LEN 0x2   /* position/length outside the block table or max_seq_len */
 #define QMLA_STATUS_TIMEOUT 0x4   /* a bounded device wait gave up; output invalid */
 
-/* Bytes of one 64-token block in `format` (20736 / 12544 / 73728), 0 for an
- * unknown format.  Layout in the comment at the top of this file. */
+/* Bytes of one 64-token block in `format` (20736 / 12544 / 73728 / 19712 /
+ * 11520), 0 for an unknown format.  Layout in the comment at the top of this file. */
 size_t qmla_block_bytes(int format);
 
 /* qmla_append - quantize and pack new tokens into the paged cache.

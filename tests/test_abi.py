@@ -44,7 +44,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_block_bytes(lib):
-    assert [lib.qmla_block_bytes(f) for f in (0, 1, 2, 3, -1)] == [20736, 12544, 73728, 0, 0]
+    assert [lib.qmla_block_bytes(f) for f in (0, 1, 2, 3, 4, 5, -1)] == [
+        20736, 12544, 73728, 19712, 11520, 0, 0]
 
 
 def test_error_strings(lib):

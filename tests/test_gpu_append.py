@@ -13,7 +13,7 @@ from bit_mla_kv_qmla_gb300.cache import PagedCache, build_cache
 from helpers import oracle_pool_for_seq
 
 pytestmark = pytest.mark.gpu
-FMTS = ["C4R4", "C2R4", "BF16"]
+FMTS = ["C4R4", "C2R4", "BF16", "C4R2", "C2R2"]
 
 
 def _seq_blocks(pool: np.ndarray, row: np.ndarray, n: int, bb: int) -> np.ndarray:
@@ -44,7 +44,8 @@ def test_append_tiny_workload_bitexact(fmt):
 
 @pytest.mark.parametrize("cfg,fmt,seqs", [(1, "C4R4", [0, 31]), (2, "C4R4", [5]),
                                           (3, "C2R4", [0, 17, 63]), (4, "C4R4", [2]),
-                                          (4, "C2R4", [1]), (4, "BF16", [3])])
+                                          (4, "C2R4", [1]), (4, "BF16", [3]),
+                                          (1, "C2R2", [3, 30]), (3, "C4R2", [9])])
 def test_append_full_size_sampled_bitexact(cfg, fmt, seqs):
     w = W.with_format(W.WORKLOADS[cfg], fmt)
     cache = build_cache(w, "cuda", gen_device="cuda")
@@ -97,7 +98,7 @@ def test_append_hard_values_bitexact(fmt):
     assert np.array_equal(cache.blocks.cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("fmt", ["C4R4", "C2R4"])
+@pytest.mark.parametrize("fmt", ["C4R4", "C2R4", "C2R2"])
 def test_append_incremental_equals_bulk_gpu(fmt):
     n = 130
     lat, rope = _hard_tokens(n, 4)

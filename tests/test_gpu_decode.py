@@ -16,7 +16,7 @@ from bit_mla_kv_qmla_gb300.cache import Decoder, PagedCache, build_cache
 from helpers import compare_rows, oracle_pool_for_seq, sample_heads
 
 pytestmark = pytest.mark.gpu
-FMTS = ["C4R4", "C2R4", "BF16"]
+FMTS = ["C4R4", "C2R4", "BF16", "C4R2", "C2R2"]
 
 
 def _small_workload(fmt, heads, seed):
@@ -111,7 +111,8 @@ def test_decode_tiny_workload(fmt):
 
 
 FULL = [(1, "C4R4", [0, 19], 6), (2, "C4R4", [3], 8), (3, "C2R4", [0, 40, 63], 6),
-        (4, "C4R4", [1], 8), (4, "C2R4", [2], 6), (4, "BF16", [0], 6), (1, "BF16", [5, 30], 16)]
+        (4, "C4R4", [1], 8), (4, "C2R4", [2], 6), (4, "BF16", [0], 6), (1, "BF16", [5, 30], 16),
+        (1, "C2R2", [4], 8), (2, "C4R2", [11], 6)]
 
 
 @pytest.mark.parametrize("cfg,fmt,seqs,nheads", FULL)
