@@ -566,6 +566,33 @@ def footprint_sweep():
             "gain_vs_bf16": {f: round(mx[f] / mx["BF16"], 3) for f in mx}}
 
 
+def capacity_sweep(rates):
+    """The cache-pressure mechanism behind the pages' whole-job result,
+    replayed by bit_mla_kv_qmla_gb300.capacity: 512 requests with prompts
+    uniform in [8K, 128K] tokens and 1024 generated tokens each, at most 256
+    running, cache budgets of 8, 16 and 32 GB.  Per format and budget:
+    preemptions, tokens recomputed on readmission, decode steps and mean
+    running sequences; where this run measured the format's decode rate at 16
+    heads (tokens attended/s), the job's decode time at that rate."""
+    import bit_mla_kv_qmla_gb300 as q
+    from bit_mla_kv_qmla_gb300 import capacity as C
+    reqs = C.synthetic_requests(512, 8192, 131072, 1024, seed=1)
+    out = {}
+    for gb in (8, 16, 32):
+        row = {}
+        for f in ("BF16", "C4R4", "C2R4"):
+            r = C.simulate(q.qmla_block_bytes(f), gb * 10 ** 9, reqs, 256)
+            ent = {k: r[k] for k in ("preemptions", "recomputed_tokens", "steps")}
+            ent["mean_running"] = round(r["mean_running"], 1)
+            if rates.get(f):
+                ent["decode_s_at_measured_rate"] = round(r["attended_tokens"] / rates[f], 3)
+            row[f] = ent
+        out[f"{gb}GB"] = row
+    return {"requests": "512, prompts U[8192, 131072], 1024 generated, <= 256 running",
+            "rates_tokens_per_s": {f: round(v) for f, v in rates.items() if v},
+            "by_budget": out}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle arm (reference and cpu_baseline)
 # ---------------------------------------------------------------------------
@@ -722,6 +749,9 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "footprint_150GB": footprint_sweep(),
+        "capacity_sim": capacity_sweep({
+            "C4R4": tok / el if (w.fmt == "C4R4" and w.heads == 16) else None,
+            "BF16": (also or {}).get("bf16_b32_h16_l8192_append1", {}).get("tokens_per_s")}),
         "also": also,
     }
     print(json.dumps(line))
