@@ -182,7 +182,8 @@ def test_decode_bad_block_and_length_are_flagged():
 
 
 @pytest.mark.parametrize("fmt,heads,q_len", [("C4R4", 16, 8), ("C2R4", 16, 8), ("BF16", 16, 8),
-                                             ("C4R4", 64, 2), ("C4R4", 8, 2), ("C4R4", 16, 2)])
+                                             ("C4R4", 64, 2), ("C4R4", 8, 2), ("C4R4", 16, 2),
+                                             ("C2R2", 16, 4)])
 def test_decode_multi_query(fmt, heads, q_len):
     """Multi-token query decode (q_len queries per sequence, causal) against the
     oracle, every row: 16 x 8 and 64 x 2 query rows run on the 128-head
