@@ -32,40 +32,45 @@ __device__ __forceinline__ float warp_max(float v) {
 // M = max(1, ceil((mx - Z*u) / (levels*u))) such that |Z| <= 2047 and
 // |Z + levels*M| <= 2047.  Every dequantized value (Z + c*M)*u is then exactly
 // a binary16 number, so the tensor cores multiply exactly the value the
-// quantizer defines.  Warp uniform.  Every step is exact, so no rounding mode
-// matters and no binary64 division is needed: mn and mx (bfloat16 values)
-// scale by 2^-E exactly in binary64, Z is the floor of the scaled minimum,
-// N = mx/u - Z is an exact binary64 difference (N >= 0 since Z <= mn/u <=
-// mx/u), and M = ceil(N / levels) = ceil(ceil(N) / levels) is an integer
-// division.
+// quantizer defines.  Warp uniform.  Every step is exact in binary32 and
+// integer arithmetic (no binary64, which is slow here): mn and mx are
+// bfloat16 values, so mn/u and mx/u (|.| <= 2^12 for E >= ilogb(m) - 11, m =
+// max |x|, or a division by at most 32 at the top exponent) are binary32
+// numbers -- bfloat16's 8 significant bits stay above binary32's subnormal
+// granularity even after that division; Z is the floor of the scaled
+// minimum; since Z is an integer, ceil(mx/u - Z) = ceil(mx/u) - Z = N >= 0
+// (Z <= mn/u <= mx/u); and M = ceil(N / levels) is an integer division.
 __device__ __forceinline__ void group_grid(float mn, float mx, int levels, float& s, float& z) {
-  const double d = double(mx) - double(mn);  // exact
-  int E = (d > 0.0) ? max(-24, ilogb(d) - 12) : -24;
-  // No E below ilogb(m) - 11, m = max(|mn|, |mx|), can pass: u <= m/4096 puts
-  // |Z| or Z + levels*M (>= mx/u) above 2047.  Starting there skips those
-  // iterations and finds the same E.
+  // start: a lower bound on the exponent found (the difference rounded down)
+  const float d = __fsub_rd(mx, mn);
+  int E = (d > 0.0f) ? max(-24, ilogbf(d) - 12) : -24;
+  // No E below ilogb(m) - 11 can pass: u <= m/4096 puts |Z| or Z + levels*M
+  // (>= mx/u) above 2047.  Starting there skips those iterations and finds
+  // the same E.
   const float m = fmaxf(fabsf(mn), fabsf(mx));
   if (m > 0.0f) E = max(E, min(ilogbf(m) - 11, 5));
   for (;; ++E) {
-    const double a_mn = ldexp(double(mn), -E), a_mx = ldexp(double(mx), -E);  // exact
-    const double Zd = floor(a_mn);
-    // |Z| and N beyond 2^40 fail the bounds below anyway; clamp before the
-    // integer conversion
-    const int64_t Z = int64_t(fmin(fmax(Zd, -1099511627776.0), 1099511627776.0));
-    const double N = fmin(a_mx - Zd, 1099511627776.0);  // exact below the clamp
-    int64_t M = (int64_t(ceil(N)) + levels - 1) / levels;
+    const float inv_u = __int_as_float((127 - E) << 23);  // 2^-E, a normal number
+    const float a_mn = mn * inv_u, a_mx = mx * inv_u;     // exact
+    // magnitudes beyond 2^29 fail the bounds below anyway; clamp before the
+    // integer conversions so that N stays an int
+    const int Z = int(fminf(fmaxf(floorf(a_mn), -536870912.0f), 536870912.0f));
+    const int C = int(fminf(fmaxf(ceilf(a_mx), -536870912.0f), 536870912.0f));
+    const int N = C - Z;  // = ceil(mx/u - Z) while unclamped
+    int M = (N + levels - 1) / levels;
     if (M < 1) M = 1;
-    const bool ok = (Z >= -2047 && Z <= 2047) && (Z + levels * M <= 2047);
+    const bool ok = (Z >= -2047 && Z <= 2047) && (int64_t(Z) + int64_t(levels) * M <= 2047);
     if (ok || E >= 5) {
-      int64_t Zc = Z, Mc = M;
+      int Zc = Z, Mc = M;
       if (!ok) {  // outside the |x| < 32768 precondition: clamp into range
         Zc = Z < -2047 ? -2047 : (Z > 2047 ? 2047 : Z);
-        const int64_t mmax = (2047 - Zc) / levels;
+        const int mmax = (2047 - Zc) / levels;
         Mc = M > mmax ? mmax : M;
         if (Mc < 1) Mc = 1;
       }
-      z = ldexpf(float(Zc), E);  // exact
-      s = ldexpf(float(Mc), E);  // exact
+      const float u = __int_as_float((127 + E) << 23);  // 2^E
+      z = float(Zc) * u;  // exact
+      s = float(Mc) * u;  // exact
       return;
     }
   }

@@ -34,7 +34,8 @@
  *             M = max(1, ceil((mx - Z*u) / (levels*u)))   (quotient rounded up)
  *             satisfy |Z| <= 2047 and |Z + levels*M| <= 2047; the search starts
  *             at E = max(-24, ilogb(mx - mn) - 12) (difference rounded down),
- *             a lower bound, and uses binary64 arithmetic
+ *             a lower bound; every step is exact (no rounding decides E, Z
+ *             or M)
  *   z       = Z*u, s = M*u, both stored as binary16 (exactly)
  *   code_i  = clamp(rint((x_i - z) / s), 0, levels), the subtraction and the
  *             division in binary32 rounded to nearest-even, rint half to even
