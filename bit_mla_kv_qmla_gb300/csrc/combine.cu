@@ -3,7 +3,8 @@
 // Each piece i of a sequence holds a normalized partial O_i and its LSE_i;
 // the full result is LSE = ln sum_i exp(LSE_i) and
 // O = sum_i exp(LSE_i - LSE) * O_i, written as bfloat16 O and binary32 LSE
-// (computed as sum_i w_i O_i / sum_i w_i with w_i = exp(LSE_i - max_j LSE_j)).
+// (computed as sum_i w_i O_i / sum_i w_i with w_i = exp(LSE_i - max_j LSE_j),
+// the maximum kept running over the pieces).
 // A sequence with no piece (length 0) gets O = 0 and LSE = -inf.
 // Grid (batch, heads), 128 threads, 4 channels per thread.
 
@@ -26,25 +27,45 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int heads,
   const float* plse = ws.part_lse + int64_t(base) * heads + h;
   const float4* po = reinterpret_cast<const float4*>(ws.part_o + (int64_t(base) * heads + h) * kDc) + tid;
   const int64_t ostride = int64_t(heads) * kDc / 4;  // float4s from one piece to the next
-  // two passes, each unrolled so that several pieces' loads are in flight:
-  // the maximum LSE, then the weighted sum of the partial outputs
-  float m = -INFINITY;
-#pragma unroll 4
-  for (int i = 0; i < n; ++i) m = fmaxf(m, plse[int64_t(i) * heads]);
+  // one pass with a running maximum, eight pieces at a time: the LSEs and
+  // partial outputs of up to eight pieces are loaded before any is used, so a
+  // sequence with at most eight pieces costs one round of loads
+  constexpr int kU = 8;
+  float m = -INFINITY, sum = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < n; i0 += kU) {
+    float l[kU];
+    float4 o[kU];
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const bool in = i0 + k < n;
+      l[k] = in ? plse[int64_t(i0 + k) * heads] : -INFINITY;
+      o[k] = in ? po[int64_t(i0 + k) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mc = m;
+#pragma unroll
+    for (int k = 0; k < kU; ++k) mc = fmaxf(mc, l[k]);
+    if (mc > -INFINITY) {
+      const float sc = __expf(m - mc);  // 0 while m is still -inf
+      sum *= sc;
+      acc.x *= sc;
+      acc.y *= sc;
+      acc.z *= sc;
+      acc.w *= sc;
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const float wgt = __expf(l[k] - mc);  // 0 for empty pieces and padding
+        sum += wgt;
+        acc.x = fmaf(wgt, o[k].x, acc.x);
+        acc.y = fmaf(wgt, o[k].y, acc.y);
+        acc.z = fmaf(wgt, o[k].z, acc.z);
+        acc.w = fmaf(wgt, o[k].w, acc.w);
+      }
+      m = mc;
+    }
+  }
   float L = -INFINITY;
   if (m > -INFINITY) {
-    float sum = 0.0f;
-#pragma unroll 4
-    for (int i = 0; i < n; ++i) {
-      const float wgt = __expf(plse[int64_t(i) * heads] - m);
-      const float4 o = po[int64_t(i) * ostride];
-      sum += wgt;
-      acc.x = fmaf(wgt, o.x, acc.x);
-      acc.y = fmaf(wgt, o.y, acc.y);
-      acc.z = fmaf(wgt, o.z, acc.z);
-      acc.w = fmaf(wgt, o.w, acc.w);
-    }
     const float inv = 1.0f / sum;
     acc.x *= inv;
     acc.y *= inv;
