@@ -706,7 +706,8 @@ def main():
                 "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "format": w.fmt, "batch": w.batch,
-                           "heads": w.heads, "seq_len": w.seq_len},
+                           "heads": w.heads, "seq_len": w.seq_len,
+                           "append_per_step": max(1, w.n_append)},
                 "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                                  "sample": sample},
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -737,7 +738,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": res["dtype"], "data": "synthetic (seeded, bit_mla_kv_qmla_gb300/workloads.py)",
         "config": {"workload": w.name, "format": w.fmt, "batch": w.batch, "heads": w.heads,
-                   "seq_len": w.seq_len, "append_per_step": max(1, w.n_append),
+                   "seq_len": w.seq_len,
+                   "append_per_step": max(1, w.n_append) if args.config == 1 else w.n_append,
                    "launch": ("CUDA graph replay of each step's library calls" if res["graph"]
                               else "eager library calls"),
                    "l2": (f"rotating {res['copies']} cache copies of "
