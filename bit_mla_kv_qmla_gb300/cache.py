@@ -9,7 +9,7 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (BLOCK_TOKENS, _fmt, qmla_append_advance, qmla_block_bytes, qmla_decode,
+from . import (_fmt, qmla_append_advance, qmla_block_bytes, qmla_decode,
                qmla_decode_multi, qmla_decode_workspace_bytes)
 from . import workloads as W
 
