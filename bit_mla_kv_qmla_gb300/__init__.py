@@ -88,7 +88,7 @@ def qmla_decode_workspace_bytes(fmt, batch: int, heads: int, max_seq_len: int) -
 
 
 def qmla_decode(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r, scale: float,
-                out, lse, workspace, status, stream=None) -> None:
+                out, lse, workspace, status, stream=None, _entry="qmla_decode") -> None:
     """Absorbed-query MLA decode; writes out [B][H][512] bf16 and lse [B][H] f32."""
     B, H = int(q_c.shape[0]), int(q_c.shape[1])
     if block_table.shape[0] < B or seq_lens.numel() < B or tuple(q_r.shape[:2]) != (B, H):
@@ -96,12 +96,21 @@ def qmla_decode(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r, 
     if tuple(out.shape) != (B, H, D_C) or tuple(lse.shape) != (B, H):
         raise ValueError("out / lse shapes do not match the queries")
     num_blocks = blocks.numel() // qmla_block_bytes(fmt)
-    code = _lib.load().qmla_decode(
+    code = getattr(_lib.load(), _entry)(
         _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
         _p(seq_lens), int(max_seq_len), B, H, _p(q_c), _p(q_r), float(scale), _p(out), _p(lse),
         _p(workspace), int(workspace.numel() * workspace.element_size()), _p(status),
         _stream(stream))
-    _check("qmla_decode", code)
+    _check(_entry, code)
+
+
+def qmla_decode_timeout_test(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r,
+                             scale: float, out, lse, workspace, status, stream=None) -> None:
+    """Test hook of the bounded device waits (qmla.h): qmla_decode whose
+    16-head kernel withholds one barrier arrival, so that its waits run out
+    and QMLA_STATUS_TIMEOUT is set; out / lse are not valid afterwards."""
+    qmla_decode(fmt, blocks, block_table, seq_lens, max_seq_len, q_c, q_r, scale, out, lse,
+                workspace, status, stream, _entry="qmla_decode_timeout_test")
 
 
 def qmla_decode_multi(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_c, q_r,

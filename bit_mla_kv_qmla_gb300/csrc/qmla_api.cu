@@ -62,7 +62,7 @@ int decode_impl(int format, const void* blocks, int64_t num_blocks, const int32_
                 int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
                 int32_t batch, int32_t heads, int32_t q_len, int32_t q_heads, const void* q_c,
                 const void* q_r, float softmax_scale, void* out, float* lse, void* workspace,
-                size_t workspace_bytes, int32_t* status_dev, void* stream) {
+                size_t workspace_bytes, int32_t* status_dev, void* stream, int withhold = 0) {
   if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
   if (batch < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
     return QMLA_ERR_INVALID_ARG;
@@ -98,6 +98,7 @@ int decode_impl(int format, const void* blocks, int64_t num_blocks, const int32_
   a.status = status_dev;
   a.q_len = q_len;
   a.q_heads = q_len > 1 ? q_heads : 0;
+  a.withhold = withhold;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   // 16 query rows of a multi-token query step go to the CUDA-core kernel:
@@ -182,6 +183,19 @@ int qmla_decode_multi(int format, const void* blocks, int64_t num_blocks,
   return decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
                      max_seq_len, batch, heads * q_len, q_len, heads, q_c, q_r, softmax_scale,
                      out, lse, workspace, workspace_bytes, status_dev, stream);
+}
+
+int qmla_decode_timeout_test(int format, const void* blocks, int64_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t max_seq_len, int32_t batch,
+                             int32_t heads, const void* q_c, const void* q_r,
+                             float softmax_scale, void* out, float* lse, void* workspace,
+                             size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  // only the 16-head tensor-core kernel (low-bit formats) carries the hook
+  if (heads != 16 || (format != QMLA_C4R4 && format != QMLA_C2R4)) return QMLA_ERR_UNSUPPORTED;
+  return decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
+                     max_seq_len, batch, heads, 1, 0, q_c, q_r, softmax_scale, out, lse,
+                     workspace, workspace_bytes, status_dev, stream, 1);
 }
 
 int qmla_read_status(const int32_t* status_dev, void* stream) {

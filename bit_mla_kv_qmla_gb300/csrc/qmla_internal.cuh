@@ -130,6 +130,10 @@ struct DecodeArgs {
   // one query per sequence, every cached token visible.
   int q_len = 1;
   int q_heads = 0;
+  // Test hook (qmla_decode_timeout_test only): the 16-head tensor-core
+  // kernel's dequantization warps withhold their first arrival, so that the
+  // bounded waits run out and the kernel reports QMLA_STATUS_TIMEOUT.
+  int withhold = 0;
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (the

@@ -266,6 +266,22 @@ int qmla_decode_noalloc(int format, const void* blocks, int64_t num_blocks,
                         const void* q_c, const void* q_r, float softmax_scale,
                         void* out, float* lse, int32_t* status_dev, void* stream);
 
+/* qmla_decode_timeout_test - TEST HOOK for the failure path of the bounded
+ * device waits; not for production use.  Same arguments as qmla_decode, for
+ * 16 heads and the C4R4 / C2R4 formats only (else QMLA_ERR_UNSUPPORTED).  The
+ * 16-head tensor-core kernel's dequantization warps withhold one barrier
+ * arrival on each worker's first tile, so the waits behind it run out after
+ * their 1 s limit: every role of the kernel then unwinds, the kernel exits
+ * normally, QMLA_STATUS_TIMEOUT is OR-ed into *status_dev and out / lse hold
+ * no valid result.  The CUDA context stays usable.  Nothing faults, traps or
+ * hangs. */
+int qmla_decode_timeout_test(int format, const void* blocks, int64_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t max_seq_len, int32_t batch,
+                             int32_t heads, const void* q_c, const void* q_r,
+                             float softmax_scale, void* out, float* lse, void* workspace,
+                             size_t workspace_bytes, int32_t* status_dev, void* stream);
+
 /* Synchronize `stream`, read *status_dev and return QMLA_OK if it is 0,
  * QMLA_ERR_DEVICE otherwise (QMLA_ERR_CUDA if the copy failed). */
 int qmla_read_status(const int32_t* status_dev, void* stream);

@@ -31,8 +31,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["qmla_block_bytes", "qmla_append", "qmla_append_advance",
                             "qmla_decode_workspace_bytes", "qmla_decode_multi",
-                            "qmla_decode", "qmla_decode_noalloc", "qmla_read_status",
-                            "qmla_error_string"])
+                            "qmla_decode", "qmla_decode_noalloc", "qmla_decode_timeout_test",
+                            "qmla_read_status", "qmla_error_string"])
 
 
 def test_library_exports_every_declared_symbol(lib):
