@@ -112,7 +112,7 @@ def test_decode_tiny_workload(fmt):
 
 FULL = [(1, "C4R4", [0, 19], 6), (2, "C4R4", [3], 8), (3, "C2R4", [0, 40, 63], 6),
         (4, "C4R4", [1], 8), (4, "C2R4", [2], 6), (4, "BF16", [0], 6), (1, "BF16", [5, 30], 16),
-        (1, "C2R2", [4], 8), (2, "C4R2", [11], 6)]
+        (1, "C2R2", [4], 8), (2, "C4R2", [11], 6), (2, "C2R4", [7], 6), (3, "C4R4", [20, 51], 6)]
 
 
 @pytest.mark.parametrize("cfg,fmt,seqs,nheads", FULL)
