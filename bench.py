@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "low-bit MLA decode: cached tokens attended/s and % of roofline at 1 GPU"
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2**20
-TOKEN_BYTES = {"C4R4": 324, "C2R4": 196, "BF16": 1152}
+TOKEN_BYTES = {"C4R4": 324, "C2R4": 196, "BF16": 1152, "C4R2": 308, "C2R2": 180}
 FLOP_PER_TOKEN_HEAD = 2 * (576 + 512)
 IO_BYTES_PER_HEAD = 576 * 2 + 512 * 2 + 4  # q in, O out, LSE out
 DECODE_SOURCES = ["decode_tc.cu", "decode_tc16.cu", "decode_simt.cu", "plan.cuh",
