@@ -12,7 +12,12 @@ Prints ONE JSON line on rank 0.  `value` is cached tokens attended per second
 device time of the steps), aggregated over all ranks.  Inputs are synthetic
 and seeded (bit_mla_kv_qmla_gb300/workloads.py).  `--impl reference` times the
 CPU oracle on the host cores instead, on a bounded sample of the same
-workload.
+workload.  Besides the contract's keys the line carries `roofline` (the
+decode call against the measured peaks), `cpu_baseline`, `e2e` (host
+buffers, copies inside the timed region), `footprint_150GB`, `capacity_sim`
+(the cache-pressure scheduler simulation) and, unless --no-also, `also`: the
+other workloads, the multi-token query decode, the folded-transform error
+and the RoPE-at-INT2 comparison.
 """
 from __future__ import annotations
 
