@@ -606,14 +606,15 @@ class OracleRunner:
     """The oracle's step (append one token to each sampled sequence, then
     decode them with every head), on the host, single-threaded."""
 
-    def __init__(self, cfg, fmt, n_seq, max_steps):
+    def __init__(self, cfg, fmt, n_seq, max_steps, first=0):
         import numpy as np
         import oracle
         from bit_mla_kv_qmla_gb300 import workloads as W
         self.np, self.oracle, self.W = np, oracle, W
         self.w = w = W.with_format(W.WORKLOADS[cfg], fmt)
         self.n_seq = n_seq
-        lens = W.seq_lens(w)[:n_seq]
+        self.first = first  # sequences first .. first + n_seq - 1
+        lens = W.seq_lens(w)[first:first + n_seq]
         self.f = W.FORMATS[w.fmt]
         need = [(L + max_steps + 1 + 63) // 64 for L in lens]
         self.table = np.full((n_seq, max(need)), -1, np.int32)
@@ -623,22 +624,54 @@ class OracleRunner:
             k += n
         self.pool = np.zeros(k * oracle.block_bytes(self.f), np.uint8)
         for b, L in enumerate(lens):
-            lat, rope = W.tokens(w, b, L)
+            lat, rope = W.tokens(w, first + b, L)
             oracle.append(self.f, self.pool, self.table[b:b + 1], np.array([0], np.int32),
                           lat[None], rope[None])
         qc, qr = W.queries(w)
-        self.qc, self.qr = qc[:n_seq], qr[:n_seq]
+        self.qc, self.qr = qc[first:first + n_seq], qr[first:first + n_seq]
         self.cur = np.array(lens, np.int32)
         self.s = 0
         self.sample = f"{n_seq} of {w.batch} sequences x {w.heads} heads per step"
 
     def step(self):
         self.s += 1
-        lat, rope = self.W.tokens(self.w, 0, self.n_seq, offset_seed=self.s)
+        lat, rope = self.W.tokens(self.w, self.first, self.n_seq, offset_seed=self.s)
         self.oracle.append(self.f, self.pool, self.table, self.cur, lat[:, None], rope[:, None])
         self.cur = self.cur + 1
         self.oracle.decode(self.f, self.pool, self.table, self.cur, self.qc, self.qr, self.w.scale)
         return int(self.cur.sum())
+
+
+def _oracle_worker(args):
+    """One process of the multi-core oracle timing: its own runner over a
+    disjoint set of sequences, timed between two barriers."""
+    import torch
+    torch.set_num_threads(1)  # one core per process (input generation included)
+    cfg, fmt, n_seq, first, steps, warmup, barrier = args
+    r = OracleRunner(cfg, fmt, n_seq, steps + warmup, first=first)
+    for _ in range(warmup):
+        r.step()
+    barrier.wait()
+    tokens, t0 = 0, time.perf_counter()
+    for _ in range(steps):
+        tokens += r.step()
+    return tokens, time.perf_counter() - t0
+
+
+def oracle_multicore(cfg, fmt, procs, n_seq, steps, warmup):
+    """The oracle's step over procs x n_seq sequences, split over procs
+    processes (started with spawn), all timed together.  Returns (tokens
+    attended / the slowest process's time, that time)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        barrier = mgr.Barrier(procs)
+        with ctx.Pool(procs) as pool:
+            res = pool.map(_oracle_worker, [(cfg, fmt, n_seq, p * n_seq, steps, warmup, barrier)
+                                            for p in range(procs)])
+    tokens = sum(r[0] for r in res)
+    t = max(r[1] for r in res)
+    return tokens / t, t
 
 
 def cpu_baseline(cfg, fmt):
@@ -679,6 +712,8 @@ def main():
     ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
     ap.add_argument("--format", default=None, choices=["C4R4", "C2R4", "BF16"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-procs", type=int, default=1,
+                    help="--impl reference: time the oracle in this many processes")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-also", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -696,16 +731,23 @@ def main():
             return
         from bit_mla_kv_qmla_gb300 import workloads as W
         w = W.with_format(W.WORKLOADS[args.config], args.format or W.WORKLOADS[args.config].fmt)
-        r = OracleRunner(args.config, w.fmt, n_seq=2 if args.config == 1 else 1,
-                         max_steps=args.steps + args.warmup)
-        for _ in range(args.warmup):
-            r.step()
-        tokens, t0 = 0, time.perf_counter()
-        for _ in range(args.steps):
-            tokens += r.step()
-        t_all = time.perf_counter() - t0
-        v = tokens / t_all
-        sample = r.sample
+        n_seq = 2 if args.config == 1 else 1
+        procs = max(1, min(args.cpu_procs, w.batch // n_seq))
+        if procs == 1:
+            r = OracleRunner(args.config, w.fmt, n_seq=n_seq, max_steps=args.steps + args.warmup)
+            for _ in range(args.warmup):
+                r.step()
+            tokens, t0 = 0, time.perf_counter()
+            for _ in range(args.steps):
+                tokens += r.step()
+            t_all = time.perf_counter() - t0
+            v = tokens / t_all
+            sample = r.sample
+        else:
+            v, t_all = oracle_multicore(args.config, w.fmt, procs, n_seq, args.steps,
+                                        args.warmup)
+            sample = (f"{procs * n_seq} of {w.batch} sequences x {w.heads} heads per step, "
+                      f"{procs} processes of {n_seq}")
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
@@ -713,7 +755,7 @@ def main():
                 "config": {"workload": w.name, "format": w.fmt, "batch": w.batch,
                            "heads": w.heads, "seq_len": w.seq_len,
                            "append_per_step": max(1, w.n_append)},
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": procs, "kind": "oracle",
                                  "sample": sample},
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}

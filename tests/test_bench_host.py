@@ -71,3 +71,14 @@ def test_capacity_sweep_shows_the_pressure_gap():
     assert at8["BF16"]["steps"] > at8["C4R4"]["steps"]
     assert "decode_s_at_measured_rate" in at8["C4R4"]
     assert "decode_s_at_measured_rate" not in at8["C2R4"]
+
+
+def test_oracle_multicore_covers_disjoint_sequences():
+    # two processes of two sequences each: the same tokens per step as one
+    # runner over four sequences (sequence b of the workload stays sequence b)
+    v, t = bench.oracle_multicore(1, "C4R4", 2, 2, steps=1, warmup=0)
+    assert v > 0 and t > 0
+    one = bench.OracleRunner(1, "C4R4", 4, 1)
+    two = [bench.OracleRunner(1, "C4R4", 2, 1, first=f) for f in (0, 2)]
+    assert one.step() == sum(r.step() for r in two)
+    assert (one.qc[2:] == two[1].qc).all()
