@@ -17,6 +17,7 @@ D_C, D_R, GROUP, BLOCK_TOKENS = 512, 64, 64, 64
 
 QMLA_OK = 0
 QMLA_STATUS_BAD_BLOCK, QMLA_STATUS_BAD_LEN, QMLA_STATUS_TIMEOUT = 0x1, 0x2, 0x4
+QMLA_STATUS_BAD_QUERY = 0x8
 
 
 class QmlaError(RuntimeError):

@@ -1,44 +1,63 @@
 // decode_tc.cu - tensor-core (tcgen05) decode over the low-bit paged cache,
-// 128 absorbed query heads.
+// 128 query heads (128 absorbed heads, or the 128 query rows of a
+// multi-token query step), and the split planner of both tensor-core decodes.
 //
 // The "native low-bit MLA attention kernel" of "QuantMLA: INT4 (and INT2) for
 // both halves of the MLA cache" (flowchart node "Low-bit kernel: dequant
 // inside attention"; "Key findings"): packed blocks are unpacked and
-// dequantized in shared memory and consumed directly by the tensor cores.
+// dequantized on chip and consumed directly by the tensor cores.
 //
-// Work split.  O for 128 heads x 512 channels in binary32 fills the whole
-// 512-column tensor memory of an SM, so one work unit runs on a cluster of
-// two CTAs: CTA r owns content channels 256r..256r+255 and RoPE channels
-// 32r..32r+31, which is exactly one contiguous half of every cache block.
-//   QK : S_r[128 heads x 64 tok] = Qc_r (A, tensor memory) x K_r^T (B, smem)
-//                                + Qr_r (A, smem)          x R_r^T (B, smem)
-//        the softmax of heads 64r..64r+63 runs on CTA r: each CTA sends the
-//        partial scores of the other CTA's heads (16 KB per tile) through
-//        cluster shared memory with asynchronous remote stores that complete
-//        on the receiver's mbarrier, adds the partials it receives for its
-//        own heads, and sends back those heads' P rows (binary16, 8 KB) with
-//        their rescale factors, so both CTAs end up with the full P tile;
-//   PV : O_r[128 x 256] += P (A, smem) x C_r (B, the same dequantized smem
-//        tile read MN-major).
-// Tensor memory per CTA: O_r cols 0-255, Qc_r cols 256-383, S double buffer
-// cols 384-511.
+// Work split.  A work unit (a range of cache blocks of one sequence, in tiles
+// of two blocks = 128 tokens) runs on a cluster of two CTAs.  CTA r
+//   * computes the scores and the softmax of heads 64r .. 64r+63 over all 576
+//     channels, tokens on the MMA's M:
+//       S^T[128 tok x 64 heads] = K[128 tok x 576] (A) x Q_r^T (B, smem),
+//     so the scores of its heads are complete in its own tensor memory and
+//     no partial score ever crosses between the CTAs;
+//   * accumulates O of all 128 heads over its half of the content channels,
+//     256r .. 256r+255, heads on M:
+//       O_r[128 heads x 256 ch] += P[128 heads x 128 tok] (A, smem) x
+//                                  C_r[128 tok x 256 ch] (B, smem),
+//     for which it needs the other CTA's P rows: 16 KB per tile and
+//     direction through cluster shared memory, with the rescale factors.
+// O of 128 heads x 512 channels in binary32 would fill all 512 columns of an
+// SM's tensor memory, which is why O is split by channel.  Each CTA
+// dequantizes all 576 channels of every token (the two CTAs read the same
+// packed blocks at the same time; the second read hits L2).
 //
-// Warp roles (14 warps): 0 bulk-copy producer, 1 MMA issuer, 2-5 softmax
-// (thread = head), 6-13 dequantization.  Dequantized operands are binary16
-// (code*scale + zero, exact by construction of the quantizer's grid);
-// queries are converted bf16 -> binary16; accumulation is binary32.
+// Operand placement (the tensor core reads shared memory at 128 B/clock, so
+// an MMA whose operands both come from shared memory at N = 64 would wait
+// for its operands; A from tensor memory avoids that):
+//   tensor memory: O_r (256 columns), S^T (64), and the A operand of QK for
+//     the content channels of the other CTA's half (4 x 32 columns), the RoPE
+//     channels (32) and one content chunk of this CTA's half (32);
+//   shared memory: Q_r^T (72 KB), P (32 KB), and a ring of seven 16 KB
+//     content chunks of this CTA's half (K for QK read K-major, the same bytes
+//     C_r for P.V read MN-major).  A tile's four chunks sit in slots 0-3
+//     (even tiles) or 3-6 (odd tiles): slot 3 is the one chunk of a tile that
+//     is written after the previous tile's P.V has released it, and the copy
+//     in tensor memory lets QK run before that.
+//
+// Pipeline: the MMA warp issues QK of tile t, then P.V of tile t-1, so the
+// softmax of tile t-1 and its P exchange overlap the tensor core's QK of
+// tile t, and the dequantization of tile t+1 overlaps the P.V of tile t-1.
+//
+// Warp roles (20 warps, five warpgroups): 0 MMA issuer (1-3 idle); 4-11
+// softmax (thread = token row of S^T; two warps per tensor-memory lane
+// quarter, 32 heads each); 12-19 dequantization (thread = token row; two
+// warps per lane quarter).  The first warpgroup hands most of its registers
+// to the other four (setmaxnreg): 48 + 120 (softmax) + 96 (dequantization)
+// per thread of each sub-partition's five warps, within the launch's 96 x 5.
+// Binary16
+// operands (exact on the quantizer's grid), binary32 accumulation.  The
+// softmax is online in base 2 with lazy rescaling: the running maximum of a
+// head only moves when a score exceeds it by more than 8 (P <= 256).  Every
+// wait is bounded in time; on timeout the CTA raises an abort flag, all
+// roles unwind and QMLA_STATUS_TIMEOUT is reported.
 //
 // The same kernel serves the uncompressed BF16 cache, the baseline the
-// low-bit formats are compared with: nothing is dequantized; the
-// "dequantization" warps load each tile's rows straight from HBM (256-bit
-// loads, one tile ahead), convert them bfloat16 -> binary16 (exact for cache
-// values in binary16's normal range; P, the other operand of P.V, needs
-// binary16's 11 significant bits at long contexts) and store them into the
-// swizzled operand tile; the producer warp has nothing to do.
-// The softmax is online in base 2 with lazy rescaling: O and l are rescaled
-// only when a tile's maximum exceeds the running one by more than 8
-// (P <= 256).  Every wait is bounded in time; on timeout the CTA raises an
-// abort flag, all roles unwind, and QMLA_STATUS_TIMEOUT is reported.
+// low-bit formats are compared with: the rows are loaded and converted
+// bfloat16 -> binary16 instead of dequantized.
 
 #include <cfloat>
 
@@ -103,43 +122,62 @@ using namespace ptx;
 using namespace tc;
 
 // ---------------------------------------------------------------- layout
-constexpr int kThreads = 448;
-constexpr int kMmaWarp = 1;
-constexpr int kSoftmaxWarp0 = 2;
-constexpr int kDequantWarp0 = 6;
-constexpr int kDequantThreads = 256;
+constexpr int kThreads = 20 * 32;
+constexpr int kMmaWarp = 0;
+constexpr int kSmxWarp0 = 4;   // 8 softmax warps (warpgroups 1-2)
+constexpr int kDqWarp0 = 12;   // 8 dequantization warps (warpgroups 3-4)
+constexpr uint32_t kRegsIdle = 48, kRegsSmx = 120, kRegsDq = 96;
+static_assert(128 * kRegsIdle + 256 * kRegsSmx + 256 * kRegsDq <= kThreads * 96 &&
+                  kRegsDq == 96,
+              "register split within the launch allocation (96 per thread at 20 warps)");
 
+// tensor memory (32-bit columns)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
+constexpr uint32_t kColO = 0;    // O_r: lane = head, 256 channels
+constexpr uint32_t kColS = 256;  // S^T: lane = token, 64 heads
+constexpr uint32_t kColK = 320;  // K units u = 0..5 at 320 + 32u, lane = token, binary16 pairs:
+                                 // 0-3 the other half's content chunks, 4 this half's late
+                                 // chunk, 5 the 64 RoPE channels
 
-constexpr uint32_t kSmQr = 0;                        // [128 heads][128 B] SW128, 16 KB
-constexpr uint32_t kSmK = 16384;                     // 2 x K tile
-constexpr uint32_t kChunk = 8192;                    // [64 tok][64 ch] fp16 SW128
-constexpr uint32_t kKTile = 5 * kChunk;              // 4 content chunks + RoPE chunk
-constexpr uint32_t kStages = 4;                      // bulk-copy ring depth
-constexpr uint32_t kSmStage = kSmK + 2 * kKTile;     // kStages x staging
-constexpr uint32_t kStage = 10240 + 256;             // largest half + RoPE scale/zero
-constexpr uint32_t kSmX = kSmStage + kStages * kStage;  // 2 x received partial scores
-constexpr uint32_t kX = 64 * 64 * 4;                 // [64 own heads][64 tok] fp32
-constexpr uint32_t kSmPt = kSmX + 2 * kX;            // 2 x P tile
-constexpr uint32_t kPt = 128 * 128;                  // [128 heads][64 tok] fp16 SW128
-constexpr uint32_t kSmAlpha = kSmPt + 2 * kPt;       // 2 x [64] received rescale factors
-constexpr uint32_t kSmLx = kSmAlpha + 2 * 256;       // [64] received row sums (per piece)
-constexpr uint32_t kPx = 64 * 128 + 64 * 4;          // P rows + rescale factors per tile
-constexpr uint32_t kSmBar = kSmLx + 256;
-constexpr uint32_t kNumBars = 27;
+// shared memory
+constexpr uint32_t kQChunk = 8192;  // [64 heads][64 ch] binary16, SW128 K-major
+constexpr uint32_t kAtom = 16384;   // [128 rows][64] binary16, SW128
+constexpr uint32_t kSmQ = 0;                                  // 9 chunks: content 0-7, RoPE
+constexpr uint32_t kSmP = kSmQ + 9 * kQChunk;                 // 2 atoms: heads 0-63, 64-127
+constexpr uint32_t kSmRing = kSmP + 2 * kAtom;                // 7 content chunk slots
+constexpr uint32_t kSlots = 7;
+constexpr uint32_t kSmAlphaIn = kSmRing + kSlots * kAtom;     // [64] the peer's rescale factors
+constexpr uint32_t kSmAlphaOwn = kSmAlphaIn + 256;            // [64] this CTA's factors
+constexpr uint32_t kSmM = kSmAlphaOwn + 256;                  // [64] running maxima (log2 units)
+constexpr uint32_t kSmLIn = kSmM + 256;                       // [64] the peer's row sums
+constexpr uint32_t kSmLOwn = kSmLIn + 256;                    // [64] this CTA's row sums
+constexpr uint32_t kSmRed = kSmLOwn + 256;                    // [4 lane quarters][64] partials
+constexpr uint32_t kSmBar = kSmRed + 1024;
+enum : uint32_t {
+  B_Q_FULL = 0,  // this piece's queries staged (8 dequantization warps)
+  B_S_FULL,      // QK of a tile complete (commit)
+  B_S_EMPTY,     // the softmax has read the scores (8 softmax warps)
+  B_KT_FULL,     // the tensor-memory K units of a tile written (8 dequantization warps)
+  B_KT_EMPTY,    // QK of a tile complete: K units and Q free (commit)
+  B_RING_FULL,   // a tile's three early ring chunks written (8 dequantization warps)
+  B_LATE_FULL,   // a tile's late ring chunk (slot 3) written (4 dequantization warps)
+  B_PV_DONE,     // P.V of a tile complete: its ring slots and P free (commit)
+  B_P_FULL,      // a tile's P complete and O rescaled (8 softmax warps)
+  B_PX_FULL,     // the peer's P rows and factors arrived (1 arming arrival + bytes)
+  B_PFREE,       // the peer's P.V of a tile complete (8 remote arrivals)
+  B_O_EMPTY,     // the epilogue has read O (8 softmax warps)
+  B_LX_FULL,     // the peer's row sums arrived (1 arming arrival + bytes)
+  B_DRAIN,
+  kNumBars
+};
 constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
-constexpr uint32_t kSmBytes = kSmAbort + 60;
-constexpr uint32_t kSmDyn = kSmBytes + 1024;         // slack for 1 KB alignment
-
-// barrier indices
-enum : uint32_t {
-  B_STAGE_FULL = 0, B_STAGE_EMPTY = 4, B_K_FULL = 8, B_K_EMPTY = 10, B_S_FULL = 12,
-  B_P_FULL = 14, B_PV_DONE = 16, B_X_FULL = 18, B_X_EMPTY = 20, B_Q_FULL = 22, B_DRAIN = 23,
-  B_PX_FULL = 24, B_LX_FULL = 26
-};
-static_assert(kSmPt % 1024 == 0, "SW128 operand tiles are 1 KB aligned");
+constexpr uint32_t kSmBytes = kSmAbort + 12;
+constexpr uint32_t kSmDyn = kSmBytes + 1024;  // slack for 1 KB alignment
+constexpr uint32_t kPx = 128 * 64 * 2 + 64 * 4;  // P rows + rescale factors per tile
+static_assert(kSmP % 1024 == 0 && kSmRing % 1024 == 0, "SW128 operand tiles are 1 KB aligned");
+static_assert(kSmBar % 8 == 0, "mbarrier alignment");
+static_assert(kSmDyn <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* r) {
   asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -147,45 +185,187 @@ __device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* r) {
                  "=r"(r[6]), "=r"(r[7])
                : "l"(p));
 }
+__device__ __forceinline__ void ld_nc_v4(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "l"(p));
+}
+__device__ __forceinline__ uint32_t ld_nc_b32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// Either half of a binary16 pair is infinite.
+__device__ __forceinline__ bool h2_inf(uint32_t w) {
+  return (w & 0x7fffu) == 0x7c00u || (w & 0x7fff0000u) == 0x7c000000u;
+}
+
+// Packed codes of one 64-channel unit of one token: a content group (INT4:
+// 8 words, INT2: 4) or the 64 RoPE channels (INT4: two 16-byte halves), and
+// the (scale, zero) word.  A zero scale/zero word makes every value +0,
+// whatever the codes hold.
+struct Unit {
+  uint32_t c[8];
+  uint32_t sz;
+};
+template <int kCBits>
+__device__ __forceinline__ void load_content(Unit& u, const uint8_t* blk, const Geom& G, int grp,
+                                             int slot) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) u.c[e] = 0u;
+  u.sz = 0u;
+  if (blk == nullptr) return;
+  const uint8_t* half = blk + (grp >> 2) * G.half;
+  const int g = grp & 3;
+  if (kCBits == 4)
+    ld_nc_v8(half + g * 2048 + slot * 32, u.c);
+  else
+    ld_nc_v4(half + g * 1024 + slot * 16, u.c);
+  u.sz = ld_nc_b32(half + G.sz_off + (g * 64 + slot) * 4);
+}
+__device__ __forceinline__ void load_rope(Unit& u, const uint8_t* blk, const Geom& G, int slot) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) u.c[e] = 0u;
+  u.sz = 0u;
+  if (blk == nullptr) return;
+  ld_nc_v4(blk + G.rope_off + slot * 16, u.c);
+  ld_nc_v4(blk + G.half + G.rope_off + slot * 16, u.c + 4);
+  u.sz = ld_nc_b32(blk + G.rope_sz_off + slot * 4);
+}
+// Channels 32*part .. 32*part+31 of a unit as 16 binary16 pairs (channel
+// 2k low, 2k+1 high).  The RoPE unit is INT4 in both halves.
+template <int kCBits>
+__device__ __forceinline__ void dq_half(const Unit& u, int part, uint32_t (&v)[16]) {
+  __half2 s2, z2;
+  split_sz(u.sz, s2, z2);
+  if (kCBits == 4) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) dq_int4(u.c[4 * part + w], s2, z2, v + 4 * w);
+  } else {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) dq_int2(u.c[2 * part + w], s2, z2, v + 8 * w);
+  }
+}
+// BF16 cache: 64 bfloat16 values of a content group row (128 B) or of the
+// RoPE key (two 64 B halves), converted to binary16 pairs.
+__device__ __forceinline__ void load_bf16_content(uint32_t (&w)[32], const uint8_t* blk,
+                                                  const Geom& G, int grp, int slot) {
+  if (blk == nullptr) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) w[e] = 0u;
+    return;
+  }
+  const uint8_t* row = blk + (grp >> 2) * G.half + ((grp & 3) * 64 + slot) * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ld_nc_v8(row + 32 * i, w + 8 * i);
+}
+__device__ __forceinline__ void load_bf16_rope(uint32_t (&w)[32], const uint8_t* blk,
+                                               const Geom& G, int slot) {
+  if (blk == nullptr) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) w[e] = 0u;
+    return;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint8_t* row = blk + h * G.half + G.rope_off + slot * 64;
+    ld_nc_v8(row, w + 16 * h);
+    ld_nc_v8(row + 32, w + 16 * h + 8);
+  }
+}
+__device__ __forceinline__ void bf16_to_f16(uint32_t (&w)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    w[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+}
+// 64 channels into row `row_off` (precomputed row offset) of an SW128 atom.
+__device__ __forceinline__ void st_row64(unsigned char* atom, uint32_t row_off, int sw7,
+                                         const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+    *reinterpret_cast<uint4*>(atom + row_off + ((g ^ sw7) << 4)) =
+        make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+}
+// Channels 32*part .. 32*part+31 of a row.
+__device__ __forceinline__ void st_row32(unsigned char* atom, uint32_t row_off, int sw7, int part,
+                                         const uint32_t (&v)[16]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    *reinterpret_cast<uint4*>(atom + row_off + (((4 * part + g) ^ sw7) << 4)) =
+        make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+}
+// A unit of packed codes, dequantized, into tensor-memory columns `col`
+// (32 columns, lane = this thread's token row) or into a ring atom row.
+template <int kCBits>
+__device__ __forceinline__ void unit_to_tmem(const Unit& u, bool rope, uint32_t taddr) {
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+    uint32_t v[16];
+    if (rope)
+      dq_half<4>(u, part, v);
+    else
+      dq_half<kCBits>(u, part, v);
+    tmem_st16(taddr + 16u * part, v);
+  }
+}
+template <int kCBits>
+__device__ __forceinline__ void unit_to_ring(const Unit& u, unsigned char* atom, uint32_t row_off,
+                                             int sw7) {
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+    uint32_t v[16];
+    dq_half<kCBits>(u, part, v);
+    st_row32(atom, row_off, sw7, part, v);
+  }
+}
+
+// Tiles of the worker: tile i of piece s covers blocks j0 + 2i, j0 + 2i + 1.
+__device__ __forceinline__ int piece_tiles(const int4& pc) {
+  return pc.z > pc.y ? (pc.z - pc.y + 1) >> 1 : 0;
+}
 
 // ---------------------------------------------------------------- kernel
-template <bool kBF16>
+template <int kCBits>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc128_kernel(DecodeArgs a) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb0 = smem_u32(sm);
   auto BAR = [&](uint32_t i) { return sb0 + kSmBar + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmAbort);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
-  const Geom G = geom(a.fmt);
+  constexpr bool kBF16 = kCBits == 16;
+  const Geom G = geom(kCBits == 4 ? QMLA_C4R4 : kCBits == 2 ? QMLA_C2R4 : QMLA_BF16);
 
   if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < kStages; ++i) {
-      mbar_init(BAR(B_STAGE_FULL + i), 1);
-      mbar_init(BAR(B_STAGE_EMPTY + i), kDequantThreads / 32);
-    }
-    for (uint32_t i = 0; i < 2; ++i) {
-      mbar_init(BAR(B_K_FULL + i), kDequantThreads / 32);
-      mbar_init(BAR(B_K_EMPTY + i), 1);
-      mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_P_FULL + i), 128);
-      mbar_init(BAR(B_PV_DONE + i), 1);
-      mbar_init(BAR(B_X_FULL + i), 1);
-      mbar_init(BAR(B_X_EMPTY + i), 64);  // the peer's 64 owning threads
-      mbar_init(BAR(B_PX_FULL + i), 1);
-    }
-    mbar_init(BAR(B_Q_FULL), 128);
-    mbar_init(BAR(B_DRAIN), 1);
+    mbar_init(BAR(B_Q_FULL), 8);
+    mbar_init(BAR(B_S_FULL), 1);
+    mbar_init(BAR(B_S_EMPTY), 8);
+    mbar_init(BAR(B_KT_FULL), 8);
+    mbar_init(BAR(B_KT_EMPTY), 1);
+    mbar_init(BAR(B_RING_FULL), 8);
+    mbar_init(BAR(B_LATE_FULL), 4);
+    mbar_init(BAR(B_PV_DONE), 1);
+    mbar_init(BAR(B_P_FULL), 8);
+    mbar_init(BAR(B_PX_FULL), 1);
+    mbar_init(BAR(B_PFREE), 8);
+    mbar_init(BAR(B_O_EMPTY), 8);
     mbar_init(BAR(B_LX_FULL), 1);
+    mbar_init(BAR(B_DRAIN), 1);
     // the first exchanges are expected before the peer can send them
-    mbar_arrive_expect_tx(BAR(B_X_FULL + 0), kX);
-    mbar_arrive_expect_tx(BAR(B_X_FULL + 1), kX);
-    mbar_arrive_expect_tx(BAR(B_PX_FULL + 0), kPx);
-    mbar_arrive_expect_tx(BAR(B_PX_FULL + 1), kPx);
+    mbar_arrive_expect_tx(BAR(B_PX_FULL), kPx);
     mbar_arrive_expect_tx(BAR(B_LX_FULL), 256);
     *abort_flag = 0;
     fence_mbar_init();
@@ -201,501 +381,602 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kSmTslot);
   const int2 wr = a.ws.wrange[pair];
 
-  if (warp == 0 && !kBF16) {
-    // ------------------------------------------------------------ producer
-    uint32_t t = 0;
-    bool ok = true;
-    for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
-      for (int jb = pc.y; ok && jb < pc.z; jb += 32) {
-        const int n = min(32, pc.z - jb);
-        const int32_t my_blk =
-            (lane < n) ? a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + jb + lane] : -1;
-        for (int k = 0; k < n; ++k, ++t) {
-          const int32_t blk = __shfl_sync(0xffffffffu, my_blk, k);
-          bool got = true;
-          if (lane == 0) {
-            const uint32_t st = t % kStages, par = (t / kStages) & 1u;
-            got = mbar_wait(BAR(B_STAGE_EMPTY + st), par ^ 1u, abort_flag, kWaitNs);
-            if (got) {
-              const uint32_t dst = sb0 + kSmStage + st * kStage;
-              if (blk >= 0 && blk < a.num_blocks) {
-                const unsigned char* src = a.blocks + int64_t(blk) * G.block;
-                mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), uint32_t(G.half) + 256u);
-                bulk_g2s(dst, src + rank * G.half, uint32_t(G.half), BAR(B_STAGE_FULL + st));
-                bulk_g2s(dst + G.half, src + G.rope_sz_off, 256u, BAR(B_STAGE_FULL + st));
-              } else {
-                set_status(a.status, QMLA_STATUS_BAD_BLOCK);
-                mbar_arrive_expect_tx(BAR(B_STAGE_FULL + st), 0u);
-              }
-            }
-          }
-          if (!warp_ok(got)) {
-            ok = false;
-            break;
-          }
-        }
-      }
-    }
-    // copies still in flight must land before the CTA can exit
-    if (lane == 0)
-      for (uint32_t u = (t >= kStages ? t - kStages : 0); u < t; ++u)
-        wait_noabort(BAR(B_STAGE_FULL + u % kStages), (u / kStages) & 1u);
-  } else if (warp == kMmaWarp) {
+  if (warp < kSmxWarp0) {
+    // the first warpgroup (all four warps at this one instruction) gives up
+    // registers; only its first warp has work
+    setmaxnreg_dec<kRegsIdle>();
+  }
+  if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop converged and an elected lane issues each
-    // instruction (single-lane issue behind waits and branches costs several
-    // times more per MMA).
-    const uint32_t idesc_qk = idesc_f16(128, 64, false, false);
-    const uint32_t idesc_pv = idesc_f16(128, 256, false, true);
+    // instruction.
+    const uint32_t idq = idesc_f16(128, 64, false, false);
+    const uint32_t idp = idesc_f16(128, 256, true, true);
     // operand descriptors; an offset advances the 16-byte address field
-    const uint64_t dKt = smem_desc(sb0 + kSmK, 16, 1024, kSwizzle128B);
-    const uint64_t dCt = smem_desc(sb0 + kSmK, kChunk, 1024, kSwizzle128B);
-    const uint64_t dQr = smem_desc(sb0 + kSmQr, 16, 1024, kSwizzle128B);
-    const uint64_t dPt = smem_desc(sb0 + kSmPt, 16, 1024, kSwizzle128B);
-    uint32_t t = 0, piece = 0;
+    const uint64_t dQ = smem_desc(sb0 + kSmQ, 16, 1024, kSwizzle128B);
+    const uint64_t dK = smem_desc(sb0 + kSmRing, 16, 1024, kSwizzle128B);
+    const uint64_t dV = smem_desc(sb0 + kSmRing, kAtom, 1024, kSwizzle128B);
+    const uint64_t dP = smem_desc(sb0 + kSmP, kAtom, 1024, kSwizzle128B);
+    uint32_t t = 0, pq = 0;
     bool ok = true;
-    auto issue_pv = [&](uint32_t tt, bool first) {
-      const uint32_t sb = tt & 1u;
+    // P.V of the previous tile, issued after QK of the next one
+    bool pend = false, pfirst = false;
+    uint32_t pt = 0, ppq = 0;
+    auto issue_pv = [&]() -> bool {
+      bool got = mbar_wait(BAR(B_P_FULL), pt & 1u, abort_flag, kWaitNs);
+      got = got && mbar_wait(BAR(B_LATE_FULL), pt & 1u, abort_flag, kWaitNs);
+      // the first tile of a piece overwrites O: the last piece's epilogue has read it
+      if (pfirst && ppq > 0)
+        got = got && mbar_wait(BAR(B_O_EMPTY), (ppq - 1) & 1u, abort_flag, kWaitNs);
+      if (!warp_ok(got)) return false;
+      tc_fence_after();
+      const uint32_t vbase = (pt & 1u) ? 3u * kAtom : 0u;
 #pragma unroll
-      for (uint32_t kk = 0; kk < 4; ++kk) {
-        mma_ss_warp(tbase + kColO, dPt + ((sb * kPt + kk * 32) >> 4),
-                    dCt + ((sb * kKTile + kk * 2048) >> 4), idesc_pv,
-                    (first && kk == 0) ? 0u : 1u);
-      }
-      mma_commit_warp(BAR(B_PV_DONE + sb));
-      mma_commit_warp(BAR(B_K_EMPTY + sb));
+      for (uint32_t kt = 0; kt < 8; ++kt)
+        mma_ss_warp(tbase + kColO, dP + ((kt * 2048u) >> 4), dV + ((vbase + kt * 2048u) >> 4), idp,
+                    (pfirst && kt == 0) ? 0u : 1u);
+      mma_commit_warp(BAR(B_PV_DONE));
+      return true;
     };
     for (int s = wr.x; ok && s <= wr.y; ++s) {
       const int4 pc = a.ws.pieces[s];
-      if (pc.z <= pc.y) continue;
-      if (!warp_ok(mbar_wait(BAR(B_Q_FULL), piece & 1u, abort_flag, kWaitNs))) break;
-      ++piece;
-      tc_fence_after();
-      for (int j = pc.y; j < pc.z; ++j, ++t) {
-        const uint32_t sb = t & 1u, par = (t >> 1) & 1u;
-        bool got = mbar_wait(BAR(B_K_FULL + sb), par, abort_flag, kWaitNs);
-        got = got && (t < 2 || mbar_wait(BAR(B_PV_DONE + sb), par ^ 1u, abort_flag, kWaitNs));
+      const int nt = piece_tiles(pc);
+      if (nt == 0) continue;
+      if (!warp_ok(mbar_wait(BAR(B_Q_FULL), pq & 1u, abort_flag, kWaitNs))) {
+        ok = false;
+        break;
+      }
+      for (int i = 0; i < nt; ++i, ++t) {
+        bool got = t == 0 || mbar_wait(BAR(B_S_EMPTY), (t - 1) & 1u, abort_flag, kWaitNs);
+        got = got && mbar_wait(BAR(B_KT_FULL), t & 1u, abort_flag, kWaitNs);
         if (!warp_ok(got)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t dk = dKt + ((sb * kKTile) >> 4);
-        const uint32_t d = tbase + kColS + 64 * sb;
+        const uint32_t odd = t & 1u;
+        const uint32_t lc = odd ? 0u : 3u;  // this half's chunk in slot 3
+        // QK from tensor memory: the other half's content, the late chunk, RoPE
+#pragma unroll 1
+        for (uint32_t u = 0; u < 6; ++u) {
+          const uint32_t qc = u < 4 ? 4u * peer + u : (u == 4 ? 4u * rank + lc : 8u);
 #pragma unroll
-        for (uint32_t kc = 0; kc < 16; ++kc)
-          mma_ts_warp(d, tbase + kColQ + 8 * kc, dk + (((kc >> 2) * kChunk + (kc & 3) * 32) >> 4),
-                      idesc_qk, kc > 0 ? 1u : 0u);
-#pragma unroll
-        for (uint32_t kr = 0; kr < 2; ++kr)
-          mma_ss_warp(d, dQr + ((kr * 32) >> 4), dk + ((4 * kChunk + kr * 32) >> 4), idesc_qk, 1u);
-        mma_commit_warp(BAR(B_S_FULL + sb));
-        if (j > pc.y) {
-          const uint32_t tp = t - 1;
-          if (!warp_ok(mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag,
-                                 kWaitNs))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(tp, j - 1 == pc.y);
+          for (uint32_t ks = 0; ks < 4; ++ks)
+            mma_ts_warp(tbase + kColS, tbase + kColK + 32u * u + 8u * ks,
+                        dQ + ((qc * kQChunk + 32u * ks) >> 4), idq, (u | ks) ? 1u : 0u);
         }
+        // QK from the ring: this half's three early chunks
+        if (!warp_ok(mbar_wait(BAR(B_RING_FULL), t & 1u, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = odd ? 3u : 0u;
+#pragma unroll 1
+        for (uint32_t e = 0; e < 3; ++e) {
+          const uint32_t c = e + odd;
+#pragma unroll
+          for (uint32_t ks = 0; ks < 4; ++ks)
+            mma_ss_warp(tbase + kColS, dK + (((base + c) * kAtom + 32u * ks) >> 4),
+                        dQ + (((4u * rank + c) * kQChunk + 32u * ks) >> 4), idq, 1u);
+        }
+        mma_commit_warp(BAR(B_S_FULL));
+        mma_commit_warp(BAR(B_KT_EMPTY));
+        if (pend && !issue_pv()) {
+          ok = false;
+          break;
+        }
+        pend = true;
+        pt = t;
+        pfirst = i == 0;
+        ppq = pq;
       }
-      if (!ok) break;
-      const uint32_t tp = t - 1;
-      if (!warp_ok(mbar_wait(BAR(B_P_FULL + (tp & 1u)), (tp >> 1) & 1u, abort_flag, kWaitNs)))
-        break;
-      tc_fence_after();
-      issue_pv(tp, pc.z - 1 == pc.y);
+      ++pq;
     }
+    if (ok && pend) issue_pv();
     // no MMA may be in flight when tensor memory is released
     mma_commit_warp(BAR(B_DRAIN));
     if (lane == 0) wait_noabort(BAR(B_DRAIN), 0);
     __syncwarp();
-  } else if (warp >= kSoftmaxWarp0 && warp < kDequantWarp0) {
+  } else if (warp < kSmxWarp0) {
+    // idle warps of the first warpgroup
+  } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ softmax
-    // thread = head h (tensor-memory lane).  CTA r owns heads 64r..64r+63
-    // (lane quarters 2r, 2r+1): their softmax runs here.  The other two warps
-    // send the peer the partial scores of the peer's heads and then take the
-    // peer's P rows and rescale factors for them.
+    setmaxnreg_inc<kRegsSmx>();
+    // thread = token row tt of S^T (its lane quarter's tensor-memory lanes);
+    // the warp holds 32 of this CTA's 64 heads.  For O (lane = head) the same
+    // thread stands for head tt.
+    const int sw = warp - kSmxWarp0;  // 0..7
     const uint32_t quad = uint32_t(warp & 3);
-    const int h = int(quad * 32) + lane;
-    const bool own = (quad >> 1) == rank;
-    const int hx = h & 63;  // row of h in the exchange buffers of its owner
+    const int hh = sw >> 2;            // this CTA's heads 32hh .. 32hh+31
+    const int tt = int(quad) * 32 + lane;
     const uint32_t lane_base = (quad * 32u) << 16;
+    const bool o_own = (quad >> 1) == rank;  // O rows of this lane quarter: this CTA's heads
+    const int oh = int(quad & 1u) * 32 + lane;  // head within its owner's 64
     const float c2 = a.scale * 1.4426950408889634f;  // scores to log2 units
-    // row h of a P tile (SW128 K-major, 64 tokens = 128 B)
-    const uint32_t prow = kSmPt + uint32_t(h >> 3) * 1024u + uint32_t(h & 7) * 128u;
-    uint32_t t = 0, piece = 0;
-    bool ok = true;
-    for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
-      const int b = pc.x;
-      if (pc.z <= pc.y) {  // no block: an empty partial (the planner produces none)
-        for (int c = 0; c < 256; ++c) a.ws.part_o[(int64_t(s) * 128 + h) * kDc + 256 * rank + c] = 0.f;
-        if (own) a.ws.part_lse[int64_t(s) * 128 + h] = -INFINITY;
-        continue;
-      }
-      const int L = seq_len_clamped(a, b);
-      // queries of this piece: Qc half -> tensor memory, Qr half -> smem
-      {
-        const __nv_bfloat16* qrow = a.q_c + (int64_t(b) * 128 + h) * kDc + 256 * rank;
+    float* m_run = reinterpret_cast<float*>(sm + kSmM);
+    float* red = reinterpret_cast<float*>(sm + kSmRed);
+    float* al_own = reinterpret_cast<float*>(sm + kSmAlphaOwn);
+    const float* al_in = reinterpret_cast<const float*>(sm + kSmAlphaIn);
+    float* l_own = reinterpret_cast<float*>(sm + kSmLOwn);
+    const float* l_in = reinterpret_cast<const float*>(sm + kSmLIn);
+    const uint32_t prow = kSmP + rank * kAtom + uint32_t(tt >> 3) * 1024u + uint32_t(tt & 7) * 128u;
+    auto rescale_o = [&](float al) {
+      // this warp's 128 of the 256 O columns of row tt
 #pragma unroll 1
-        for (int c0 = 0; c0 < 256; c0 += 64) {
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4*>(qrow + c0 + 8 * i);
-            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              w[4 * i + k] = pack_half2(__uint_as_float(in[k] << 16),
-                                        __uint_as_float(in[k] & 0xffff0000u));
-          }
-          tmem_st32(tbase + lane_base + kColQ + c0 / 2, w);
-        }
-        const __nv_bfloat16* rrow = a.q_r + (int64_t(b) * 128 + h) * kDr + 32 * rank;
-        unsigned char* qr = sm + kSmQr + (h >> 3) * 1024 + (h & 7) * 128;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint4 v = *reinterpret_cast<const uint4*>(rrow + 8 * g);
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            o[k] = pack_half2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xffff0000u));
-          *reinterpret_cast<uint4*>(qr + ((g ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(BAR(B_Q_FULL));
-      }
-      float m_run = -INFINITY, l_run = 0.0f;  // own heads
-      uint32_t vmask = 0;
-      for (int j = pc.y; j < pc.z; ++j, ++t) {
-        if (((j - pc.y) & 31) == 0) vmask = valid_mask(a, b, j, pc.z);
-        const uint32_t sb = t & 1u, par = (t >> 1) & 1u;
-        if (!warp_ok(mbar_wait(BAR(B_S_FULL + sb), par, abort_flag, kWaitNs))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        float sv[64];
-        {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tbase + lane_base + kColS + 64 * sb, r0);
-          tmem_ld32(tbase + lane_base + kColS + 64 * sb + 32, r1);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            sv[i] = __uint_as_float(r0[i]);
-            sv[32 + i] = __uint_as_float(r1[i]);
-          }
-        }
-        float alpha = 1.0f;
-        if (!own) {
-          // --- the peer's head: send its partial scores, take back P and the
-          // rescale factor.  (The peer writes P into this CTA's tile only after
-          // these scores arrive, and they leave only after this CTA's QK of
-          // tile t, i.e. after its P.V of tile t-2 read that tile parity.)
-          if (!warp_ok(mbar_wait<true>(BAR(B_X_EMPTY + sb), par ^ 1u, abort_flag, kWaitNs))) {
-            ok = false;
-            break;
-          }
-          {
-            const uint32_t xrow = mapa(sb0 + kSmX + sb * kX + uint32_t(hx) * 256u, peer);
-            const uint32_t pbar = mapa(BAR(B_X_FULL + sb), peer);
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              st_async_v4(xrow + ((uint32_t(q) ^ uint32_t(hx & 15)) << 4), sv[4 * q],
-                          sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3], pbar);
-          }
-          if (!warp_ok(mbar_wait<true>(BAR(B_PX_FULL + sb), par, abort_flag, kWaitNs))) {
-            ok = false;
-            break;
-          }
-          alpha = *reinterpret_cast<const volatile float*>(sm + kSmAlpha + sb * 256 + hx * 4);
-          // expect this buffer's next exchange (tile t+2) before the peer can
-          // send it: the peer sends it only after scores this thread sends
-          // later have arrived
-          if (hx == 0) mbar_arrive_expect_tx(BAR(B_PX_FULL + sb), kPx);
-        } else {
-          // --- this CTA's head: add the peer's partial, softmax, send P back
-          if (!warp_ok(mbar_wait<true>(BAR(B_X_FULL + sb), par, abort_flag, kWaitNs))) {
-            ok = false;
-            break;
-          }
-          const uint32_t xrow = kSmX + sb * kX + uint32_t(hx) * 256u;
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float4 v = *reinterpret_cast<const float4*>(sm + xrow + ((q ^ (hx & 15)) << 4));
-            sv[4 * q] += v.x;
-            sv[4 * q + 1] += v.y;
-            sv[4 * q + 2] += v.z;
-            sv[4 * q + 3] += v.w;
-          }
-          // this CTA's buffer sb is read: expect the exchange two tiles ahead
-          // and tell the peer it may send it
-          if (hx == 0) mbar_arrive_expect_tx(BAR(B_X_FULL + sb), kX);
-          mbar_arrive_remote(mapa(BAR(B_X_EMPTY + sb), peer));
-
-          // tokens of this tile head h may see (its query's prefix in a
-          // multi-token query decode)
-          const int nvalid =
-              ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, visible_tokens(a, h, L) - j * kT) : 0;
-#pragma unroll
-          for (int i = 0; i < 64; ++i) sv[i] *= c2;
-          if (nvalid < 64) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) sv[i] = (i < nvalid) ? sv[i] : -INFINITY;
-          }
-          float mx8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            mx8[k] = fmaxf(fmaxf(fmaxf(sv[8 * k], sv[8 * k + 1]), fmaxf(sv[8 * k + 2], sv[8 * k + 3])),
-                           fmaxf(fmaxf(sv[8 * k + 4], sv[8 * k + 5]), fmaxf(sv[8 * k + 6], sv[8 * k + 7])));
-          }
-          const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-          if (mt > m_run + 8.0f) {
-            alpha = exp2f(m_run - mt);
-            m_run = mt;
-          }
-          l_run *= alpha;
-          uint32_t pk[32];
-          float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          const float msub = (mt == -INFINITY) ? 0.0f : m_run;  // all masked: every p is 0
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2_approx(sv[2 * i] - msub);
-            const float p1 = ex2_approx(sv[2 * i + 1] - msub);
-            ls4[i & 3] += p0 + p1;
-            pk[i] = pack_half2(p0, p1);
-          }
-          l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-          // P row h into this CTA's tile and the peer's, the factor to the peer
-          const uint32_t pl = prow + sb * kPt;
-          const uint32_t pr = mapa(sb0 + pl, peer);
-          const uint32_t pbar = mapa(BAR(B_PX_FULL + sb), peer);
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint32_t off = uint32_t((g ^ (h & 7)) << 4);
-            *reinterpret_cast<uint4*>(sm + pl + off) =
-                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-            st_async_u32x4(pr + off, pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3], pbar);
-          }
-          st_async_f32(mapa(sb0 + kSmAlpha + sb * 256 + hx * 4, peer), alpha, pbar);
-        }
-        // rescale this CTA's O rows of head h (its 256 channels) when the
-        // maximum moved; the P.V products of tile t-1 must have landed first
-        if (__any_sync(0xffffffffu, alpha != 1.0f) && j > pc.y) {
-          const uint32_t tp = t - 1;
-          if (!warp_ok(mbar_wait(BAR(B_PV_DONE + (tp & 1u)), (tp >> 1) & 1u, abort_flag,
-                                 kWaitNs))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(tbase + lane_base + kColO + c0, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tbase + lane_base + kColO + c0, o);
-          }
-          tmem_wait_st();
-        }
-        // this tile's P rows (written here or by the peer) reach the tensor
-        // cores through the async proxy
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(BAR(B_P_FULL + sb));
-      }
-      if (!ok) break;
-      // epilogue: normalized partial O (this CTA's 256 channels) and LSE
-      const uint32_t tl = t - 1;
-      if (!warp_ok(mbar_wait(BAR(B_PV_DONE + (tl & 1u)), (tl >> 1) & 1u, abort_flag, kWaitNs)))
-        break;
-      tc_fence_after();
-      float l = l_run;
-      if (own) {
-        st_async_f32(mapa(sb0 + kSmLx + hx * 4, peer), l_run, mapa(BAR(B_LX_FULL), peer));
-        a.ws.part_lse[int64_t(s) * 128 + h] =
-            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-      } else {
-        if (!warp_ok(mbar_wait<true>(BAR(B_LX_FULL), piece & 1u, abort_flag, kWaitNs))) break;
-        l = *reinterpret_cast<const volatile float*>(sm + kSmLx + hx * 4);
-        __syncwarp();
-        if (hx == 0) mbar_arrive_expect_tx(BAR(B_LX_FULL), 256);
-      }
-      ++piece;
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      float* orow = a.ws.part_o + (int64_t(s) * 128 + h) * kDc + 256 * rank;
-#pragma unroll 1
-      for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
+      for (uint32_t c0 = 128u * hh; c0 < 128u * hh + 128u; c0 += 32) {
         uint32_t o[32];
         tmem_ld32(tbase + lane_base + kColO + c0, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(orow + c0 + i) =
-              make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                          __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * al);
+        tmem_st32(tbase + lane_base + kColO + c0, o);
       }
-      tc_fence_before();
-    }
-  } else if (warp >= kDequantWarp0 && kBF16) {
-    // ------------------------------------------------------------ BF16 rows
-    // thread dt owns token tt and 16-channel segment seg of each of the 4
-    // groups of this half (and, dt < 128, a 16-channel RoPE segment); the
-    // rows of the next tile are in flight while this tile's are stored
-    const int dt = int(threadIdx.x) - kDequantWarp0 * 32;
-    const int tt = (dt >> 2) & 63, seg = dt & 3;
-    const int rtt = dt >> 1, rseg = dt & 1;  // RoPE (dt < 128)
-    uint32_t t = 0;
+      tmem_wait_st();
+    };
+    uint32_t t = 0, pq = 0;
     bool ok = true;
     for (int s = wr.x; ok && s <= wr.y; ++s) {
       const int4 pc = a.ws.pieces[s];
-      if (pc.z <= pc.y) continue;
-      const int L = seq_len_clamped(a, pc.x);
-      const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
-      // rows of block j of this CTA's half, or nullptr (past the piece or a
-      // bad block id: zeros); n = valid token rows
-      auto half_of = [&](int j, int& n) -> const uint8_t* {
-        n = 0;
-        if (j >= pc.z) return nullptr;
-        const int32_t blk = btab[j];
-        if (blk < 0 || blk >= a.num_blocks) {
-          if (dt == 0) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
-          return nullptr;
-        }
-        n = min(kT, L - j * kT);
-        return a.blocks + int64_t(blk) * G.block + rank * G.half;
-      };
-      auto load_rows = [&](const uint8_t* hb, int n, uint32_t (&c)[4][8], uint32_t (&r)[8]) {
+      const int nt = piece_tiles(pc);
+      if (nt == 0) {  // no block: an empty partial (the planner produces none)
+        for (int c = 0; c < 128; ++c)
+          a.ws.part_o[(int64_t(s) * 128 + tt) * kDc + 256 * rank + 128 * hh + c] = 0.f;
+        if (quad == 0) a.ws.part_lse[int64_t(s) * 128 + 64 * rank + 32 * hh + lane] = -INFINITY;
+        continue;
+      }
+      const int b = pc.x;
+      const int L = seq_len_clamped(a, b);
+      if (quad == 0) m_run[32 * hh + lane] = -INFINITY;
+      named_bar_sync(2, 256);
+      float l[32];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          if (hb && tt < n) {
-            ld_nc_v8(hb + (g * 64 + tt) * 128 + seg * 32, c[g]);
-          } else {
+      for (int h = 0; h < 32; ++h) l[h] = 0.0f;
+      uint32_t vmask = 0;
+      for (int i = 0; i < nt; ++i, ++t) {
+        const int jt = pc.y + 2 * i;
+        if (((2 * i) & 31) == 0) vmask = valid_mask(a, b, jt, pc.z);
+        const int j = jt + (tt >> 6);
+        const bool row_ok =
+            j < pc.z && ((vmask >> ((j - pc.y) & 31)) & 1u) && (tt & 63) < L - j * kT;
+        bool got = ok && warp_ok(mbar_wait(BAR(B_S_FULL), t & 1u, abort_flag, kWaitNs));
+        float x[32];
+        if (got) {
+          tc_fence_after();
+          uint32_t r32[32];
+          tmem_ld32(tbase + lane_base + kColS + 32u * hh, r32);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_S_EMPTY));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) c[g][e] = 0u;
+          for (int h = 0; h < 32; ++h) x[h] = row_ok ? __uint_as_float(r32[h]) * c2 : -INFINITY;
+          if (a.q_heads > 0 && row_ok) {
+            // multi-token query: the last q_len - 1 positions are not visible to every row
+            const int pos = j * kT + (tt & 63);
+            if (pos >= L - a.q_len + 1) {
+#pragma unroll
+              for (int h = 0; h < 32; ++h)
+                if (pos >= visible_tokens(a, 64 * int(rank) + 32 * hh + h, L)) x[h] = -INFINITY;
+            }
           }
-        }
-        if (dt < 128 && hb && rtt < n) {
-          ld_nc_v8(hb + G.rope_off + rtt * 64 + rseg * 32, r);
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) r[e] = 0u;
+          for (int h = 0; h < 32; ++h) x[h] = -INFINITY;
         }
-      };
-      int n_cur;
-      const uint8_t* hb_cur = half_of(pc.y, n_cur);
-      uint32_t cn[4][8], rn[8];
-      load_rows(hb_cur, n_cur, cn, rn);
-      for (int j = pc.y; j < pc.z; ++j, ++t) {
-        uint32_t cc[4][8], rc[8];
+        ok = ok && got;
+        // lazy rescale: the per-head maxima are only reduced when some score
+        // exceeds the maximum in use by more than 8; the decisions are the
+        // same in every thread.  All eight warps take every barrier below
+        // whatever their waits returned: a failed wait forces the rare path,
+        // which leaves the loop together.
+        bool over = !ok;
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) cc[g][e] = cn[g][e];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) rc[e] = rn[e];
-        int n_next;
-        const uint8_t* hb_next = half_of(j + 1, n_next);
-        load_rows(hb_next, n_next, cn, rn);
-        const uint32_t kb = t & 1u;
-        if (!warp_ok(mbar_wait(BAR(B_K_EMPTY + kb), ((t >> 1) & 1u) ^ 1u, abort_flag, kWaitNs))) {
-          ok = false;
-          break;
+        for (int h = 0; h < 32; h += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(m_run + 32 * hh + h);
+          over |= (x[h] > v.x + 8.0f) | (x[h + 1] > v.y + 8.0f) | (x[h + 2] > v.z + 8.0f) |
+                  (x[h + 3] > v.w + 8.0f);
         }
-        unsigned char* kt = sm + kSmK + kb * kKTile;
-        auto to_f16 = [](uint32_t (&w)[8]) {
+        bool rescaled = false;
+        if (named_bar_or(1, 256, over)) {
+          if (named_bar_or(1, 256, !ok)) break;
+          float mine = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            w[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
-        };
+          for (int h = 0; h < 32; ++h) {
+            const float v = warp_max(x[h]);
+            if (lane == h) mine = v;
+          }
+          red[quad * 64 + 32 * hh + lane] = mine;
+          named_bar_sync(2, 256);
+          if (quad == 0) {  // one warp per head half moves the maxima
+            const int hl = 32 * hh + lane;
+            const float mt = fmaxf(fmaxf(red[hl], red[64 + hl]), fmaxf(red[128 + hl], red[192 + hl]));
+            const float mo = m_run[hl];
+            const bool need = mt > mo + 8.0f;
+            al_own[hl] = need ? ex2_approx(mo - mt) : 1.0f;  // 0 while mo is -inf
+            if (need) m_run[hl] = mt;
+          }
+          named_bar_sync(2, 256);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          to_f16(cc[g]);
-          st_row16(kt + g * kChunk, tt, seg, cc[g]);
+          for (int h = 0; h < 32; h += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(al_own + 32 * hh + h);
+            l[h] *= f.x;
+            l[h + 1] *= f.y;
+            l[h + 2] *= f.z;
+            l[h + 3] *= f.w;
+          }
+          rescaled = i > 0;  // O holds earlier tiles of this piece
         }
-        if (dt < 128) {
-          to_f16(rc);
-          st_row16(kt + 4 * kChunk, rtt, rseg, rc);
+        // P = 2^(x - m) as binary16 pairs, row sums per head
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 mm = *reinterpret_cast<const float2*>(m_run + 32 * hh + 2 * k);
+          const float m0 = mm.x == -INFINITY ? 0.0f : mm.x;  // all masked so far: p = 0
+          const float m1 = mm.y == -INFINITY ? 0.0f : mm.y;
+          const float p0 = ex2_approx(x[2 * k] - m0);
+          const float p1 = ex2_approx(x[2 * k + 1] - m1);
+          l[2 * k] += p0;
+          l[2 * k + 1] += p1;
+          pk[k] = pack_half2(p0, p1);
+        }
+        // The P buffer is free, and O holds the previous tile, once this
+        // CTA's P.V of tile t-1 has completed; the peer's copy of this CTA's
+        // rows is free once the peer's has.
+        if (t > 0) {
+          got = warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs));
+          if (got && lane == 0) mbar_arrive_remote(mapa(BAR(B_PFREE), peer));
+          got = got && warp_ok(mbar_wait<true>(BAR(B_PFREE), (t - 1) & 1u, abort_flag, kWaitNs));
+          ok = ok && got;
+        }
+        if (!ok) continue;  // the next tile's barriers take every warp out together
+        tc_fence_after();
+        if (rescaled && o_own) {
+          const float al = al_own[oh];
+          if (__any_sync(0xffffffffu, al != 1.0f)) rescale_o(al);
+        }
+        // P row tt of this CTA's heads into its atom here and in the peer
+        {
+          const uint32_t pbar = mapa(BAR(B_PX_FULL), peer);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t off = prow + uint32_t(((4 * hh + g) ^ (tt & 7)) << 4);
+            *reinterpret_cast<uint4*>(sm + off) =
+                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            st_async_u32x4(mapa(sb0 + off, peer), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
+                           pk[4 * g + 3], pbar);
+          }
+          // rescale factors of this CTA's heads for the peer's O rows
+          if (sw == 0 && lane < 16) {
+            float4 f = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+            if (rescaled) f = *reinterpret_cast<const float4*>(al_own + 4 * lane);
+            st_async_v4(mapa(sb0 + kSmAlphaIn + 16 * lane, peer), f.x, f.y, f.z, f.w, pbar);
+          }
         }
         fence_proxy_async_smem();
+        if (!o_own) {
+          // the peer's rows and factors: rescale this CTA's O rows of the peer's heads
+          got = warp_ok(mbar_wait<true>(BAR(B_PX_FULL), t & 1u, abort_flag, kWaitNs));
+          if (got) {
+            const float al = al_in[oh];
+            if (i > 0 && __any_sync(0xffffffffu, al != 1.0f)) rescale_o(al);
+            // the peer sends the next tile's exchange only after this tile's P.V
+            if (hh == 0 && (quad & 1u) == 0 && lane == 0)
+              mbar_arrive_expect_tx(BAR(B_PX_FULL), kPx);
+            fence_proxy_async_smem();
+          }
+          ok = ok && got;
+        }
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_K_FULL + kb));
+        if (ok && lane == 0) mbar_arrive(BAR(B_P_FULL));
       }
+      // every softmax warp reaches this barrier (the loop is left together)
+      if (named_bar_or(1, 256, !ok)) {
+        ok = false;
+        break;
+      }
+      // epilogue: row sums, LSE, normalized partial O of this CTA's channels
+      bool got = warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs));
+      if (named_bar_or(1, 256, !got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float mine = 0.0f;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        const float v = warp_sum_f(l[h]);
+        if (lane == h) mine = v;
+      }
+      red[quad * 64 + 32 * hh + lane] = mine;
+      named_bar_sync(2, 256);
+      if (quad == 0) {
+        const int hl = 32 * hh + lane;
+        const float ls = (red[hl] + red[64 + hl]) + (red[128 + hl] + red[192 + hl]);
+        l_own[hl] = ls;
+        a.ws.part_lse[int64_t(s) * 128 + 64 * rank + hl] =
+            ls > 0.0f ? (m_run[hl] + log2f(ls)) * 0.6931471805599453f : -INFINITY;
+      }
+      named_bar_sync(2, 256);
+      if (sw == 0 && lane < 16) {
+        const float4 v = *reinterpret_cast<const float4*>(l_own + 4 * lane);
+        st_async_v4(mapa(sb0 + kSmLIn + 16 * lane, peer), v.x, v.y, v.z, v.w,
+                    mapa(BAR(B_LX_FULL), peer));
+      }
+      got = warp_ok(mbar_wait<true>(BAR(B_LX_FULL), pq & 1u, abort_flag, kWaitNs));
+      if (named_bar_or(1, 256, !got)) {
+        ok = false;
+        break;
+      }
+      // the peer sends the next piece's sums only after that piece's tiles
+      if (sw == 0 && lane == 0) mbar_arrive_expect_tx(BAR(B_LX_FULL), 256);
+      const float lr = o_own ? l_own[oh] : l_in[oh];
+      const float inv = lr > 0.0f ? 1.0f / lr : 0.0f;
+      float* orow = a.ws.part_o + (int64_t(s) * 128 + tt) * kDc + 256 * rank;
+#pragma unroll 1
+      for (uint32_t c0 = 128u * hh; c0 < 128u * hh + 128u; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tbase + lane_base + kColO + c0, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; k += 4)
+          *reinterpret_cast<float4*>(orow + c0 + k) =
+              make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
+                          __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_O_EMPTY));
+      ++pq;
     }
-  } else if (warp >= kDequantWarp0) {
+  } else {
     // ------------------------------------------------------------ dequant
-    const int dt = int(threadIdx.x) - kDequantWarp0 * 32;
+    // (keeps the launch's register count, kRegsDq)
+    // thread = token row tt of the tile (tensor-memory lane); rows 0-63 come
+    // from the tile's first block, 64-127 from its second.  Units per tile:
+    //   dh 0: A (tensor memory) the other half's chunks 0, 1, 2;
+    //         B (ring) this half's early chunks 0 and 1 of the tile;
+    //   dh 1: A the other half's chunk 3, this half's late chunk, RoPE;
+    //         B this half's third early chunk; C the previous tile's late
+    //         chunk into ring slot 3 (after that tile's predecessor's P.V).
+    const int dw = warp - kDqWarp0, dh = dw >> 2;
+    const uint32_t quad = uint32_t(warp & 3);
+    const int tt = int(quad) * 32 + lane, bi = tt >> 6, slot = tt & 63;
+    const uint32_t lane_base = (quad * 32u) << 16;
+    const uint32_t row_off = uint32_t(tt >> 3) * 1024u + uint32_t(tt & 7) * 128u;
+    const int sw7 = tt & 7;
+    const int qt = int(threadIdx.x) - kDqWarp0 * 32;  // 0..255
+    // block of this thread's row in tile i of piece s (nullptr: no such row,
+    // a bad block id, or a token past the sequence: read as zeros)
+    auto row_block = [&](int s, int i) -> const uint8_t* {
+      const int4 pc = a.ws.pieces[s];
+      const int j = pc.y + 2 * i + bi;
+      if (j >= pc.z) return nullptr;
+      const int32_t blk = a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + j];
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0 && (dw == 0 || dw == 2)) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
+        return nullptr;
+      }
+      return slot < seq_len_clamped(a, pc.x) - j * kT ? a.blocks + int64_t(blk) * G.block : nullptr;
+    };
+    // the next tile of the worker after tile i of piece s (s > wr.y: none)
+    auto next_tile = [&](int& s, int& i) {
+      if (i + 1 < piece_tiles(a.ws.pieces[s])) {
+        ++i;
+        return;
+      }
+      i = 0;
+      for (++s; s <= wr.y && piece_tiles(a.ws.pieces[s]) == 0; ++s) {
+      }
+    };
+    // this piece's queries (this CTA's 64 heads), binary16, SW128 K-major
+    auto stage_q = [&](int b) {
+      bool bad = false;
+#pragma unroll 1
+      for (int r0 = 0; r0 < 18; r0 += 9) {
+        uint4 qv[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const int idx = qt + 256 * (r0 + k), h = idx / 72, sg = idx % 72;
+          const int64_t hv = int64_t(b) * 128 + 64 * int(rank) + h;
+          const __nv_bfloat16* src =
+              sg < 64 ? a.q_c + hv * kDc + sg * 8 : a.q_r + hv * kDr + (sg - 64) * 8;
+          qv[k] = *reinterpret_cast<const uint4*>(src);
+        }
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const int idx = qt + 256 * (r0 + k), h = idx / 72, sg = idx % 72;
+          const uint32_t in[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o[e] = pack_half2(__uint_as_float(in[e] << 16), __uint_as_float(in[e] & 0xffff0000u));
+            bad |= h2_inf(o[e]);
+          }
+          const int c = sg >> 3, g = sg & 7;
+          unsigned char* row = sm + kSmQ + c * kQChunk + (h >> 3) * 1024 + (h & 7) * 128;
+          *reinterpret_cast<uint4*>(row + ((g ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      if (bad) set_status(a.status, QMLA_STATUS_BAD_QUERY);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_Q_FULL));
+    };
+    unsigned char* ring = sm + kSmRing;
     uint32_t t = 0;
     bool ok = true;
-    for (int s = wr.x; ok && s <= wr.y; ++s) {
-      const int4 pc = a.ws.pieces[s];
-      const int L = seq_len_clamped(a, pc.x);
-      uint32_t vmask = 0;
-      for (int j = pc.y; j < pc.z; ++j, ++t) {
-        if (((j - pc.y) & 31) == 0) vmask = valid_mask(a, pc.x, j, pc.z);
-        const uint32_t st = t % kStages, kb = t & 1u;
-        bool got = mbar_wait(BAR(B_STAGE_FULL + st), (t / kStages) & 1u, abort_flag, kWaitNs);
-        got = got && mbar_wait(BAR(B_K_EMPTY + kb), ((t >> 1) & 1u) ^ 1u, abort_flag, kWaitNs);
+    int s = wr.x, i = 0;
+    while (s <= wr.y && piece_tiles(a.ws.pieces[s]) == 0) ++s;
+    if constexpr (!kBF16) {
+      // Packed codes: the A units of a tile are loaded while the previous
+      // tile's B units are processed, the B units (and the previous tile's
+      // late chunk) while its own A units are; each set has about one QK or
+      // P.V product's time to arrive, and only one set per phase is live.
+      Unit ua[3], ub[2];
+      int ps = -1, pi = 0;  // the previous tile (its late chunk goes to slot 3)
+      auto load_a = [&](int s2, int i2, uint32_t t2) {
+        const uint8_t* blk = row_block(s2, i2);
+        if (dh == 0) {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) load_content<kCBits>(ua[k], blk, G, 4 * int(peer) + k, slot);
+        } else {
+          load_content<kCBits>(ua[0], blk, G, 4 * int(peer) + 3, slot);
+          load_content<kCBits>(ua[1], blk, G, 4 * int(rank) + ((t2 & 1u) ? 0 : 3), slot);
+          load_rope(ua[2], blk, G, slot);
+        }
+      };
+      if (s <= wr.y) load_a(s, 0, 0);
+      while (ok && s <= wr.y) {
+        const int4 pc = a.ws.pieces[s];
+        bool got = t == 0 || mbar_wait(BAR(B_KT_EMPTY), (t - 1) & 1u, abort_flag, kWaitNs);
         if (!warp_ok(got)) {
           ok = false;
           break;
         }
-        const int nvalid = ((vmask >> ((j - pc.y) & 31)) & 1u) ? min(kT, L - j * kT) : 0;
-        const unsigned char* stg = sm + kSmStage + st * kStage;
-        unsigned char* kt = sm + kSmK + kb * kKTile;
-        // content: thread dt owns token tt and 16-channel segment seg of each of
-        // the 4 groups of this half; unconditional loads, invalid tokens zeroed
+        if (i == 0) stage_q(pc.x);  // QK of the previous piece is complete
+        const uint32_t odd = t & 1u;
+        // ---- A: tensor-memory units
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const uint32_t u = dh == 0 ? uint32_t(k) : uint32_t(3 + k);
+          unit_to_tmem<kCBits>(ua[k], dh == 1 && k == 2, tbase + lane_base + kColK + 32u * u);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        // (the test hook withholds the first arrival of the first CTA of each pair)
+        if (lane == 0 && !(a.withhold && t == 0 && rank == 0)) mbar_arrive(BAR(B_KT_FULL));
+        // ---- the B units' codes, and the previous tile's late chunk (dh 1)
         {
-          const int tt = (dt >> 2) & 63, seg = dt & 3;
-          const bool valid = tt < nvalid;
+          const uint8_t* blk = row_block(s, i);
+          if (dh == 0) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            __half2 s2, z2;
-            split_sz(*reinterpret_cast<const uint32_t*>(stg + G.sz_off + (g * 64 + tt) * 4), s2,
-                     z2);
-            uint32_t v[8];
-            if (G.cbits == 4) {
-              const uint2 w = *reinterpret_cast<const uint2*>(stg + g * 2048 + tt * 32 + seg * 8);
-              dq_int4(w.x, s2, z2, v);
-              dq_int4(w.y, s2, z2, v + 4);
-            } else {
-              dq_int2(*reinterpret_cast<const uint32_t*>(stg + g * 1024 + tt * 16 + seg * 4), s2, z2,
-                      v);
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = valid ? v[k] : 0u;
-            st_row16(kt + g * kChunk, tt, seg, v);
+            for (int k = 0; k < 2; ++k)
+              load_content<kCBits>(ub[k], blk, G, 4 * int(rank) + k + int(odd), slot);
+          } else {
+            load_content<kCBits>(ub[0], blk, G, 4 * int(rank) + 2 + int(odd), slot);
+            load_content<kCBits>(ub[1], ps >= 0 ? row_block(ps, pi) : nullptr, G,
+                                 4 * int(rank) + (odd ? 3 : 0), slot);
           }
         }
-        // RoPE: 64 tokens x 2 segments of 16 channels (INT4)
-        if (dt < 128) {
-          const int tt = dt >> 1, seg = dt & 1;
-          uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (tt < nvalid) {
-            __half2 s2, z2;
-            split_sz(*reinterpret_cast<const uint32_t*>(stg + G.half + tt * 4), s2, z2);
-            const uint2 w = *reinterpret_cast<const uint2*>(stg + G.rope_off + tt * 16 + seg * 8);
-            dq_int4(w.x, s2, z2, v);
-            dq_int4(w.y, s2, z2, v + 4);
-          }
-          st_row16(kt + 4 * kChunk, tt, seg, v);
+        // ---- B: this half's early chunks into the ring (slots of tile t-2)
+        got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
+        if (!warp_ok(got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t base = odd ? 3u : 0u;
+        if (dh == 0) {
+          unit_to_ring<kCBits>(ub[0], ring + (base + odd) * kAtom, row_off, sw7);
+          unit_to_ring<kCBits>(ub[1], ring + (base + 1u + odd) * kAtom, row_off, sw7);
+        } else {
+          unit_to_ring<kCBits>(ub[0], ring + (base + 2u + odd) * kAtom, row_off, sw7);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(BAR(B_K_FULL + kb));
-          mbar_arrive(BAR(B_STAGE_EMPTY + st));
+        if (lane == 0) mbar_arrive(BAR(B_RING_FULL));
+        // ---- the next tile's A codes
+        ps = s;
+        pi = i;
+        ++t;
+        next_tile(s, i);
+        if (s <= wr.y) load_a(s, i, t);
+        // ---- C: the previous tile's late chunk into slot 3 (freed with tile t-2's P.V)
+        if (dh == 1 && t >= 2) {
+          unit_to_ring<kCBits>(ub[1], ring + 3u * kAtom, row_off, sw7);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
+        }
+      }
+      // the last tile's late chunk
+      if (ok && dh == 1 && t >= 1) {
+        load_content<kCBits>(ub[1], row_block(ps, pi), G, 4 * int(rank) + (((t - 1) & 1u) ? 0 : 3),
+                             slot);
+        const bool got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
+        if (warp_ok(got)) {
+          unit_to_ring<kCBits>(ub[1], ring + 3u * kAtom, row_off, sw7);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
+        }
+      }
+    } else {
+      // BF16 rows: loaded, converted and stored unit by unit
+      int ps = -1, pi = 0;  // the previous tile (its late chunk goes to slot 3)
+      while (ok && s <= wr.y) {
+        const int4 pc = a.ws.pieces[s];
+        bool got = t == 0 || mbar_wait(BAR(B_KT_EMPTY), (t - 1) & 1u, abort_flag, kWaitNs);
+        if (!warp_ok(got)) {
+          ok = false;
+          break;
+        }
+        if (i == 0) stage_q(pc.x);
+        const uint32_t odd = t & 1u;
+        const uint8_t* blk = row_block(s, i);
+        tc_fence_after();
+#pragma unroll 1
+        for (int k = 0; k < 3; ++k) {
+          uint32_t v[32];
+          if (dh == 1 && k == 2)
+            load_bf16_rope(v, blk, G, slot);
+          else
+            load_bf16_content(v, blk, G,
+                              dh == 0 ? 4 * int(peer) + k
+                                      : (k == 0 ? 4 * int(peer) + 3 : 4 * int(rank) + (odd ? 0 : 3)),
+                              slot);
+          bf16_to_f16(v);
+          const uint32_t u = dh == 0 ? uint32_t(k) : uint32_t(3 + k);
+          tmem_st32(tbase + lane_base + kColK + 32u * u, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_KT_FULL));
+        got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
+        if (!warp_ok(got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t base = odd ? 3u : 0u;
+#pragma unroll 1
+        for (int k = 0; k < (dh == 0 ? 2 : 1); ++k) {
+          const uint32_t c = (dh == 0 ? uint32_t(k) : 2u) + odd;
+          uint32_t v[32];
+          load_bf16_content(v, blk, G, 4 * int(rank) + int(c), slot);
+          bf16_to_f16(v);
+          st_row64(ring + (base + c) * kAtom, row_off, sw7, v);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_RING_FULL));
+        if (dh == 1 && t >= 1) {
+          uint32_t v[32];
+          load_bf16_content(v, row_block(ps, pi), G, 4 * int(rank) + ((t - 1) & 1u ? 0 : 3), slot);
+          bf16_to_f16(v);
+          st_row64(ring + 3u * kAtom, row_off, sw7, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
+        }
+        ps = s;
+        pi = i;
+        ++t;
+        next_tile(s, i);
+      }
+      if (ok && dh == 1 && t >= 1) {
+        const bool got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
+        if (warp_ok(got)) {
+          uint32_t v[32];
+          load_bf16_content(v, row_block(ps, pi), G, 4 * int(rank) + ((t - 1) & 1u ? 0 : 3), slot);
+          bf16_to_f16(v);
+          st_row64(ring + 3u * kAtom, row_off, sw7, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
         }
       }
     }
@@ -703,7 +984,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && *abort_flag) set_status(a.status, QMLA_STATUS_TIMEOUT);
+  if (*abort_flag) {
+    if (threadIdx.x == 0) set_status(a.status, QMLA_STATUS_TIMEOUT);
+    // Unwinding: the peer may have sent rows or sums this CTA never waited
+    // for.  Give stores still in flight time to land before the cluster
+    // barrier lets either CTA leave.
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 100000ull) {
+    }
+  }
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -714,14 +1003,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_decode_tc128(const DecodeArgs& a, cudaStream_t stream) {
-  static int smem_attr_done[kMaxDevices], smem_attr_done_bf16[kMaxDevices];
-  cudaError_t e = launch_plan(a, stream);
+  static int done4[kMaxDevices], done2[kMaxDevices], done16[kMaxDevices];
+  DecodeArgs b = a;
+  // A second piece costs a worker about one tile (the queries' staging and
+  // the epilogue); the split charges it two blocks.
+  b.piece_cost = 2;
+  cudaError_t e = launch_plan(b, stream);
   if (e != cudaSuccess) return e;
-  const bool bf16 = a.fmt == QMLA_BF16;
-  auto kernel = bf16 ? decode_tc128_kernel<true> : decode_tc128_kernel<false>;
-  e = ensure_smem_attr(kernel, int(kSmDyn), bf16 ? smem_attr_done_bf16 : smem_attr_done);
+  auto kernel = a.fmt == QMLA_C4R4   ? decode_tc128_kernel<4>
+                : a.fmt == QMLA_C2R4 ? decode_tc128_kernel<2>
+                                     : decode_tc128_kernel<16>;
+  e = ensure_smem_attr(kernel, int(kSmDyn),
+                       a.fmt == QMLA_C4R4 ? done4 : a.fmt == QMLA_C2R4 ? done2 : done16);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(a);
+  kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(b);
   return cudaGetLastError();
 }
 

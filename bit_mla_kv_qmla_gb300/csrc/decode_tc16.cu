@@ -378,18 +378,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
       }
     };
     auto q_store = [&](const uint4 (&qv)[kSeg]) {
+      bool bad = false;  // a query value beyond binary16's range
 #pragma unroll
       for (int k = 0; k < kSeg; ++k) {
         const int i = qi0 + 128 * k, h = i / 72, sgm = i % 72;
         const uint32_t in[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
         uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
+        for (int e = 0; e < 4; ++e) {
           o[e] = pack_half2(__uint_as_float(in[e] << 16), __uint_as_float(in[e] & 0xffff0000u));
+          bad |= (o[e] & 0x7fffu) == 0x7c00u || (o[e] & 0x7fff0000u) == 0x7c000000u;
+        }
         const int c = sgm >> 3, g = sgm & 7;
         unsigned char* row = sm + kSmQ + c * 2048 + (h >> 3) * 1024 + (h & 7) * 128;
         *reinterpret_cast<uint4*>(row + ((g ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
+      if (bad) set_status(a.status, QMLA_STATUS_BAD_QUERY);
       fence_proxy_async_smem();
       mbar_arrive(BAR(B_Q_FULL));
     };

@@ -191,8 +191,9 @@ int qmla_decode_timeout_test(int format, const void* blocks, int64_t num_blocks,
                              int32_t heads, const void* q_c, const void* q_r,
                              float softmax_scale, void* out, float* lse, void* workspace,
                              size_t workspace_bytes, int32_t* status_dev, void* stream) {
-  // only the 16-head tensor-core kernel (low-bit formats) carries the hook
-  if (heads != 16 || (format != QMLA_C4R4 && format != QMLA_C2R4)) return QMLA_ERR_UNSUPPORTED;
+  // only the tensor-core kernels (low-bit formats) carry the hook
+  if ((heads != 16 && heads != 128) || (format != QMLA_C4R4 && format != QMLA_C2R4))
+    return QMLA_ERR_UNSUPPORTED;
   return decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
                      max_seq_len, batch, heads, 1, 0, q_c, q_r, softmax_scale, out, lse,
                      workspace, workspace_bytes, status_dev, stream, 1);

@@ -55,7 +55,8 @@ extern "C" int qmla_decode_noalloc(int format, const void* blocks, int64_t num_b
                                    int32_t heads, const void* q_c, const void* q_r,
                                    float softmax_scale, void* out, float* lse,
                                    int32_t* status_dev, void* stream) {
-  if (format != QMLA_C4R4 && format != QMLA_C2R4 && format != QMLA_BF16)
+  if (format != QMLA_C4R4 && format != QMLA_C2R4 && format != QMLA_BF16 &&
+      format != QMLA_C4R2 && format != QMLA_C2R2)
     return QMLA_ERR_UNSUPPORTED;
   if (batch < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
     return QMLA_ERR_INVALID_ARG;
@@ -74,13 +75,23 @@ extern "C" int qmla_decode_noalloc(int format, const void* blocks, int64_t num_b
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0)
     return QMLA_ERR_CUDA;
-  // As many workers as the decode normally uses, fewer if their partials
-  // would not fit the scratch; a batch whose merge table and one partial per
-  // sequence do not fit is rejected.
+  // As many workers as the decode normally uses, or the largest count whose
+  // partials still fit the scratch (the scratch need grows with the worker
+  // count, so a binary search finds it); a batch whose merge table and one
+  // partial per sequence do not fit is rejected.
   int workers = tc ? qmla::tc_workers(sms, heads) : qmla::simt_workers(sms);
   if (qmla::workspace_bytes(batch, heads, batch + 1) > kScratchBytes) return QMLA_ERR_CAPACITY;
-  while (workers > 1 && qmla::workspace_bytes(batch, heads, batch + workers) > kScratchBytes)
-    workers = workers / 2 > 1 ? workers / 2 : 1;
+  if (qmla::workspace_bytes(batch, heads, batch + workers) > kScratchBytes) {
+    int lo = 1, hi = workers;  // fits at lo, not at hi
+    while (hi - lo > 1) {
+      const int mid = lo + (hi - lo) / 2;
+      if (qmla::workspace_bytes(batch, heads, batch + mid) <= kScratchBytes)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    workers = lo;
+  }
 
   void* scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);

@@ -191,6 +191,19 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// Per-warpgroup register budget: every warp of a warpgroup executes the same
+// call.  Registers released by a decrease go back to the CTA's pool; an
+// increase waits until the pool holds them, so the increases of all
+// warpgroups together must fit what the decreases and the launch left.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---------------------------------------------------------------- TMEM
 // Warp-wide: allocate `ncols` (power of two >= 32) columns, address -> *dst.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -134,6 +134,8 @@ enum {
 #define QMLA_STATUS_BAD_BLOCK 0x1 /* block id < 0 or >= num_blocks; block skipped */
 #define QMLA_STATUS_BAD_LEN 0x2   /* position/length outside the block table or max_seq_len */
 #define QMLA_STATUS_TIMEOUT 0x4   /* a bounded device wait gave up; output invalid */
+#define QMLA_STATUS_BAD_QUERY 0x8 /* a query value overflows binary16 (|q| > 65504) in a
+                                     tensor-core decode; rows holding it are not valid */
 
 /* Bytes of one 64-token block in `format` (20736 / 12544 / 73728 / 19712 /
  * 11520), 0 for an unknown format.  Layout in the comment at the top of this file. */
@@ -255,10 +257,12 @@ int qmla_decode_multi(int format, const void* blocks, int64_t num_blocks,
  *     overlap on the GPU (on different streams, or concurrently from several
  *     host threads) race on it: serialize them.
  *   - When the partials of the usual split do not fit, the context is split
- *     into fewer pieces; a batch whose merge table plus one partial per
- *     sequence exceeds the array (roughly batch * heads > 16000 at 512
- *     channels) returns QMLA_ERR_CAPACITY and enqueues nothing.
- * Other errors and device status bits as for qmla_decode. */
+ *     over the largest number of workers whose partials do fit; a batch
+ *     whose merge table plus one partial per sequence exceeds the array
+ *     (roughly batch * heads > 16000 at 512 channels) returns
+ *     QMLA_ERR_CAPACITY and enqueues nothing.
+ * Formats, head counts, other errors and device status bits as for
+ * qmla_decode. */
 int qmla_decode_noalloc(int format, const void* blocks, int64_t num_blocks,
                         const int32_t* block_table, int32_t max_blocks_per_seq,
                         const int32_t* seq_lens, int32_t max_seq_len,
@@ -268,10 +272,12 @@ int qmla_decode_noalloc(int format, const void* blocks, int64_t num_blocks,
 
 /* qmla_decode_timeout_test - TEST HOOK for the failure path of the bounded
  * device waits; not for production use.  Same arguments as qmla_decode, for
- * 16 heads and the C4R4 / C2R4 formats only (else QMLA_ERR_UNSUPPORTED).  The
- * 16-head tensor-core kernel's dequantization warps withhold one barrier
- * arrival on each worker's first tile, so the waits behind it run out after
- * their 1 s limit: every role of the kernel then unwinds, the kernel exits
+ * 16 or 128 heads and the C4R4 / C2R4 formats only (else
+ * QMLA_ERR_UNSUPPORTED).  The tensor-core kernel's dequantization warps
+ * withhold a barrier arrival on the first tile (16 heads: of every worker;
+ * 128 heads: of the first CTA of every CTA pair, so the second CTA's waits
+ * on its partner run out too), so the waits behind it run out after their
+ * 1 s limit: every role of the kernel then unwinds, the kernel exits
  * normally, QMLA_STATUS_TIMEOUT is OR-ed into *status_dev and out / lse hold
  * no valid result.  The CUDA context stays usable.  Nothing faults, traps or
  * hangs. */

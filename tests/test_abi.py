@@ -118,3 +118,30 @@ def test_decode_multi_rejects_bad_arguments(lib):
 
 def test_read_status_null(lib):
     assert lib.qmla_read_status(None, None) == -1
+
+
+def test_decode_noalloc_rejects_bad_arguments(lib):
+    # every rejection below returns before the library touches the device
+    keep, p = _fake(4096)
+
+    def call(fmt=0, heads=128, batch=1, blocks=p, qc=p, out=p, lse=p, status=p, maxb=4, nb=4):
+        return lib.qmla_decode_noalloc(fmt, blocks, nb, p, maxb, p, 256, batch, heads, qc, p,
+                                       ctypes.c_float(0.1), out, lse, status, None)
+    assert call(fmt=5) == -2
+    assert call(fmt=-1) == -2
+    assert call(heads=17) == -2
+    assert call(heads=512) == -2
+    assert call(batch=-1) == -1
+    assert call(nb=0) == -1
+    assert call(blocks=None) == -1
+    assert call(qc=None) == -1
+    assert call(out=None) == -1
+    assert call(status=None) == -1
+    assert call(blocks=p + 16) == -1   # pool must be 256-byte aligned
+    assert call(qc=p + 8) == -1        # queries must be 16-byte aligned
+    assert call(lse=p + 2) == -1       # lse must be 4-byte aligned
+    assert call(maxb=0) == -1
+    assert call(batch=0) == 0          # nothing to do, nothing launched
+    # the formats qmla_decode serves are accepted up to the device query
+    for fmt in (0, 1, 2, 3, 4):
+        assert call(fmt=fmt, batch=0) == 0
