@@ -46,7 +46,7 @@
 // softmax (thread = token row of S^T; two warps per tensor-memory lane
 // quarter, 32 heads each); 12-19 dequantization (thread = token row; two
 // warps per lane quarter).  The first warpgroup hands most of its registers
-// to the other four (setmaxnreg): 48 + 120 (softmax) + 96 (dequantization)
+// to the other four (setmaxnreg): 48 + 112 (softmax) + 104 (dequantization)
 // per thread of each sub-partition's five warps, within the launch's 96 x 5.
 // Binary16
 // operands (exact on the quantizer's grid), binary32 accumulation.  The
@@ -124,11 +124,11 @@ using namespace tc;
 // ---------------------------------------------------------------- layout
 constexpr int kThreads = 20 * 32;
 constexpr int kMmaWarp = 0;
+constexpr int kXchgWarp = 1;   // moves this CTA's P rows to the peer
 constexpr int kSmxWarp0 = 4;   // 8 softmax warps (warpgroups 1-2)
 constexpr int kDqWarp0 = 12;   // 8 dequantization warps (warpgroups 3-4)
-constexpr uint32_t kRegsIdle = 48, kRegsSmx = 120, kRegsDq = 96;
-static_assert(128 * kRegsIdle + 256 * kRegsSmx + 256 * kRegsDq <= kThreads * 96 &&
-                  kRegsDq == 96,
+constexpr uint32_t kRegsIdle = 48, kRegsSmx = 112, kRegsDq = 104;
+static_assert(128 * kRegsIdle + 256 * kRegsSmx + 256 * kRegsDq <= kThreads * 96,
               "register split within the launch allocation (96 per thread at 20 warps)");
 
 // tensor memory (32-bit columns)
@@ -146,8 +146,9 @@ constexpr uint32_t kSmQ = 0;                                  // 9 chunks: conte
 constexpr uint32_t kSmP = kSmQ + 9 * kQChunk;                 // 2 atoms: heads 0-63, 64-127
 constexpr uint32_t kSmRing = kSmP + 2 * kAtom;                // 7 content chunk slots
 constexpr uint32_t kSlots = 7;
-constexpr uint32_t kSmAlphaIn = kSmRing + kSlots * kAtom;     // [64] the peer's rescale factors
-constexpr uint32_t kSmAlphaOwn = kSmAlphaIn + 256;            // [64] this CTA's factors
+constexpr uint32_t kPkt = 272;  // rescale packet: [64] factors + a 16-byte flag
+constexpr uint32_t kSmAlphaIn = kSmRing + kSlots * kAtom;     // [2][packet] from the peer
+constexpr uint32_t kSmAlphaOwn = kSmAlphaIn + 2 * kPkt;       // [64] this CTA's factors
 constexpr uint32_t kSmM = kSmAlphaOwn + 256;                  // [64] running maxima (log2 units)
 constexpr uint32_t kSmLIn = kSmM + 256;                       // [64] the peer's row sums
 constexpr uint32_t kSmLOwn = kSmLIn + 256;                    // [64] this CTA's row sums
@@ -157,14 +158,18 @@ enum : uint32_t {
   B_Q_FULL = 0,  // this piece's queries staged (8 dequantization warps)
   B_S_FULL,      // QK of a tile complete (commit)
   B_S_EMPTY,     // the softmax has read the scores (8 softmax warps)
-  B_KT_FULL,     // the tensor-memory K units of a tile written (8 dequantization warps)
-  B_KT_EMPTY,    // QK of a tile complete: K units and Q free (commit)
-  B_RING_FULL,   // a tile's three early ring chunks written (8 dequantization warps)
+  B_KT_FULL,     // [3] K unit pair k (units k, 3+k) of a tile written (8 dequantization warps)
+  B_KT_EMPTY = B_KT_FULL + 3,  // [3] the QK products reading unit pair k complete (commit)
+  B_RING_FULL = B_KT_EMPTY + 3,  // a tile's three early ring chunks written (8 dequantization warps)
   B_LATE_FULL,   // a tile's late ring chunk (slot 3) written (4 dequantization warps)
   B_PV_DONE,     // P.V of a tile complete: its ring slots and P free (commit)
-  B_P_FULL,      // a tile's P complete and O rescaled (8 softmax warps)
-  B_PX_FULL,     // the peer's P rows and factors arrived (1 arming arrival + bytes)
-  B_PFREE,       // the peer's P.V of a tile complete (8 remote arrivals)
+  B_P_LOCAL,     // this CTA's P rows of a tile written (8 softmax warps)
+  B_SRC_FREE,    // the bulk copy of those rows to the peer has read them (exchanger)
+  B_P_FULL,      // a tile's local P rows written and O rescaled (8 softmax warps)
+  B_PX_FULL,     // the peer's P rows arrived (1 arming arrival + bytes)
+  B_PFREE,       // the peer's P.V of a tile complete (1 remote arrival)
+  B_AX0,         // the peer's rescale packet of an even / odd tile arrived
+  B_AX1,         //   (1 arming arrival + bytes each)
   B_O_EMPTY,     // the epilogue has read O (8 softmax warps)
   B_LX_FULL,     // the peer's row sums arrived (1 arming arrival + bytes)
   B_DRAIN,
@@ -174,7 +179,11 @@ constexpr uint32_t kSmTslot = kSmBar + 8 * kNumBars;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
 constexpr uint32_t kSmBytes = kSmAbort + 12;
 constexpr uint32_t kSmDyn = kSmBytes + 1024;  // slack for 1 KB alignment
-constexpr uint32_t kPx = 128 * 64 * 2 + 64 * 4;  // P rows + rescale factors per tile
+constexpr uint32_t kPx = 128 * 64 * 2;  // P rows of one CTA's heads per tile
+// A head's running maximum before its first score (log2 units): finite, so
+// that scores minus it stay exact enough to find the first maximum, and far
+// below any score of binary16 operands that the softmax can represent.
+constexpr float kMaxUnset = -32768.0f;
 static_assert(kSmP % 1024 == 0 && kSmRing % 1024 == 0, "SW128 operand tiles are 1 KB aligned");
 static_assert(kSmBar % 8 == 0, "mbarrier alignment");
 static_assert(kSmDyn <= 232448, "shared memory budget");
@@ -353,19 +362,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_Q_FULL), 8);
     mbar_init(BAR(B_S_FULL), 1);
     mbar_init(BAR(B_S_EMPTY), 8);
-    mbar_init(BAR(B_KT_FULL), 8);
-    mbar_init(BAR(B_KT_EMPTY), 1);
+    for (uint32_t k = 0; k < 3; ++k) {
+      mbar_init(BAR(B_KT_FULL + k), 8);
+      mbar_init(BAR(B_KT_EMPTY + k), 1);
+    }
     mbar_init(BAR(B_RING_FULL), 8);
     mbar_init(BAR(B_LATE_FULL), 4);
     mbar_init(BAR(B_PV_DONE), 1);
+    mbar_init(BAR(B_P_LOCAL), 8);
+    mbar_init(BAR(B_SRC_FREE), 1);
     mbar_init(BAR(B_P_FULL), 8);
     mbar_init(BAR(B_PX_FULL), 1);
-    mbar_init(BAR(B_PFREE), 8);
+    mbar_init(BAR(B_PFREE), 1);
+    mbar_init(BAR(B_AX0), 1);
+    mbar_init(BAR(B_AX1), 1);
     mbar_init(BAR(B_O_EMPTY), 8);
     mbar_init(BAR(B_LX_FULL), 1);
     mbar_init(BAR(B_DRAIN), 1);
     // the first exchanges are expected before the peer can send them
     mbar_arrive_expect_tx(BAR(B_PX_FULL), kPx);
+    mbar_arrive_expect_tx(BAR(B_AX0), kPkt);
+    mbar_arrive_expect_tx(BAR(B_AX1), kPkt);
     mbar_arrive_expect_tx(BAR(B_LX_FULL), 256);
     *abort_flag = 0;
     fence_mbar_init();
@@ -405,10 +422,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto issue_pv = [&]() -> bool {
       bool got = mbar_wait(BAR(B_P_FULL), pt & 1u, abort_flag, kWaitNs);
       got = got && mbar_wait(BAR(B_LATE_FULL), pt & 1u, abort_flag, kWaitNs);
+      got = got && mbar_wait<true>(BAR(B_PX_FULL), pt & 1u, abort_flag, kWaitNs);
       // the first tile of a piece overwrites O: the last piece's epilogue has read it
       if (pfirst && ppq > 0)
         got = got && mbar_wait(BAR(B_O_EMPTY), (ppq - 1) & 1u, abort_flag, kWaitNs);
       if (!warp_ok(got)) return false;
+      // the peer sends the next tile's rows only after this tile's P.V
+      if (lane == 0) mbar_arrive_expect_tx(BAR(B_PX_FULL), kPx);
       tc_fence_after();
       const uint32_t vbase = (pt & 1u) ? 3u * kAtom : 0u;
 #pragma unroll
@@ -427,24 +447,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       for (int i = 0; i < nt; ++i, ++t) {
-        bool got = t == 0 || mbar_wait(BAR(B_S_EMPTY), (t - 1) & 1u, abort_flag, kWaitNs);
-        got = got && mbar_wait(BAR(B_KT_FULL), t & 1u, abort_flag, kWaitNs);
-        if (!warp_ok(got)) {
+        if (!warp_ok(t == 0 || mbar_wait(BAR(B_S_EMPTY), (t - 1) & 1u, abort_flag, kWaitNs))) {
           ok = false;
           break;
         }
-        tc_fence_after();
         const uint32_t odd = t & 1u;
         const uint32_t lc = odd ? 0u : 3u;  // this half's chunk in slot 3
-        // QK from tensor memory: the other half's content, the late chunk, RoPE
+        // QK from tensor memory, unit pair by unit pair as the dequantization
+        // writes them: pair k is the other half's chunk k and unit 3+k (the
+        // other half's chunk 3, this half's late chunk, RoPE); each pair is
+        // released as soon as its products complete
 #pragma unroll 1
-        for (uint32_t u = 0; u < 6; ++u) {
-          const uint32_t qc = u < 4 ? 4u * peer + u : (u == 4 ? 4u * rank + lc : 8u);
+        for (uint32_t k = 0; k < 3; ++k) {
+          if (!warp_ok(mbar_wait(BAR(B_KT_FULL + k), t & 1u, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 4; ++ks)
-            mma_ts_warp(tbase + kColS, tbase + kColK + 32u * u + 8u * ks,
-                        dQ + ((qc * kQChunk + 32u * ks) >> 4), idq, (u | ks) ? 1u : 0u);
+          for (uint32_t h = 0; h < 2; ++h) {
+            const uint32_t u = k + 3u * h;
+            const uint32_t qc = u < 4 ? 4u * peer + u : (u == 4 ? 4u * rank + lc : 8u);
+#pragma unroll
+            for (uint32_t ks = 0; ks < 4; ++ks)
+              mma_ts_warp(tbase + kColS, tbase + kColK + 32u * u + 8u * ks,
+                          dQ + ((qc * kQChunk + 32u * ks) >> 4), idq, (u | ks) ? 1u : 0u);
+          }
+          mma_commit_warp(BAR(B_KT_EMPTY + k));
         }
+        if (!ok) break;
         // QK from the ring: this half's three early chunks
         if (!warp_ok(mbar_wait(BAR(B_RING_FULL), t & 1u, abort_flag, kWaitNs))) {
           ok = false;
@@ -461,7 +492,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         dQ + (((4u * rank + c) * kQChunk + 32u * ks) >> 4), idq, 1u);
         }
         mma_commit_warp(BAR(B_S_FULL));
-        mma_commit_warp(BAR(B_KT_EMPTY));
         if (pend && !issue_pv()) {
           ok = false;
           break;
@@ -478,6 +508,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mma_commit_warp(BAR(B_DRAIN));
     if (lane == 0) wait_noabort(BAR(B_DRAIN), 0);
     __syncwarp();
+  } else if (warp == kXchgWarp) {
+    // ------------------------------------------------------------ exchanger
+    // One bulk copy per tile moves this CTA's P rows (its 64 heads, 16 KB)
+    // into the peer's P tile, once the peer's P.V of the previous tile has
+    // released it; the softmax warps never wait for the transfer.
+    const uint32_t src = sb0 + kSmP + rank * kAtom;
+    const uint32_t dst = mapa(src, peer);
+    const uint32_t pbar = mapa(BAR(B_PX_FULL), peer);
+    uint32_t t = 0;
+    bool ok = true;
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int nt = piece_tiles(a.ws.pieces[s]);
+      for (int i = 0; i < nt; ++i, ++t) {
+        bool got = mbar_wait(BAR(B_P_LOCAL), t & 1u, abort_flag, kWaitNs);
+        got = got && (t == 0 || mbar_wait<true>(BAR(B_PFREE), (t - 1) & 1u, abort_flag, kWaitNs));
+        if (!warp_ok(got)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          bulk_s2c(dst, src, kPx, pbar);
+          bulk_commit_and_wait_read();
+          mbar_arrive(BAR(B_SRC_FREE));
+        }
+        __syncwarp();
+        // this CTA's P.V of tile t has read the peer's rows: the peer may send the next
+        if (!warp_ok(mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_remote(mapa(BAR(B_PFREE), peer));
+      }
+    }
   } else if (warp < kSmxWarp0) {
     // idle warps of the first warpgroup
   } else if (warp < kDqWarp0) {
@@ -497,7 +560,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float* m_run = reinterpret_cast<float*>(sm + kSmM);
     float* red = reinterpret_cast<float*>(sm + kSmRed);
     float* al_own = reinterpret_cast<float*>(sm + kSmAlphaOwn);
-    const float* al_in = reinterpret_cast<const float*>(sm + kSmAlphaIn);
     float* l_own = reinterpret_cast<float*>(sm + kSmLOwn);
     const float* l_in = reinterpret_cast<const float*>(sm + kSmLIn);
     const uint32_t prow = kSmP + rank * kAtom + uint32_t(tt >> 3) * 1024u + uint32_t(tt & 7) * 128u;
@@ -527,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int b = pc.x;
       const int L = seq_len_clamped(a, b);
-      if (quad == 0) m_run[32 * hh + lane] = -INFINITY;
+      if (quad == 0) m_run[32 * hh + lane] = kMaxUnset;
       named_bar_sync(2, 256);
       float l[32];
 #pragma unroll
@@ -540,63 +602,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool row_ok =
             j < pc.z && ((vmask >> ((j - pc.y) & 31)) & 1u) && (tt & 63) < L - j * kT;
         bool got = ok && warp_ok(mbar_wait(BAR(B_S_FULL), t & 1u, abort_flag, kWaitNs));
-        float x[32];
-        if (got) {
+        // d = score in log2 units minus the running maximum of its head
+        float d[32];
+        auto load_d = [&]() {
           tc_fence_after();
           uint32_t r32[32];
           tmem_ld32(tbase + lane_base + kColS + 32u * hh, r32);
           tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(B_S_EMPTY));
 #pragma unroll
-          for (int h = 0; h < 32; ++h) x[h] = row_ok ? __uint_as_float(r32[h]) * c2 : -INFINITY;
-          if (a.q_heads > 0 && row_ok) {
+          for (int h = 0; h < 32; h += 4) {
+            const float4 m = *reinterpret_cast<const float4*>(m_run + 32 * hh + h);
+            d[h] = fmaf(__uint_as_float(r32[h]), c2, -m.x);
+            d[h + 1] = fmaf(__uint_as_float(r32[h + 1]), c2, -m.y);
+            d[h + 2] = fmaf(__uint_as_float(r32[h + 2]), c2, -m.z);
+            d[h + 3] = fmaf(__uint_as_float(r32[h + 3]), c2, -m.w);
+          }
+          if (!row_ok) {
+#pragma unroll
+            for (int h = 0; h < 32; ++h) d[h] = -INFINITY;
+          } else if (a.q_heads > 0) {
             // multi-token query: the last q_len - 1 positions are not visible to every row
             const int pos = j * kT + (tt & 63);
             if (pos >= L - a.q_len + 1) {
 #pragma unroll
               for (int h = 0; h < 32; ++h)
-                if (pos >= visible_tokens(a, 64 * int(rank) + 32 * hh + h, L)) x[h] = -INFINITY;
+                if (pos >= visible_tokens(a, 64 * int(rank) + 32 * hh + h, L)) d[h] = -INFINITY;
             }
           }
+        };
+        if (got) {
+          load_d();
         } else {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) x[h] = -INFINITY;
+          for (int h = 0; h < 32; ++h) d[h] = -INFINITY;
         }
         ok = ok && got;
-        // lazy rescale: the per-head maxima are only reduced when some score
-        // exceeds the maximum in use by more than 8; the decisions are the
-        // same in every thread.  All eight warps take every barrier below
-        // whatever their waits returned: a failed wait forces the rare path,
-        // which leaves the loop together.
-        bool over = !ok;
+        // lazy rescale: a head's maximum only moves when one of its scores
+        // exceeds it by more than 8 (an unset maximum is kMaxUnset, below any
+        // score); the decisions are the same in every thread.  All eight
+        // warps take every barrier below whatever their waits returned: a
+        // failed wait forces the rare path, which leaves the loop together.
+        float dmax = d[0];
 #pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(m_run + 32 * hh + h);
-          over |= (x[h] > v.x + 8.0f) | (x[h + 1] > v.y + 8.0f) | (x[h + 2] > v.z + 8.0f) |
-                  (x[h + 3] > v.w + 8.0f);
-        }
+        for (int h = 1; h < 32; ++h) dmax = fmaxf(dmax, d[h]);
         bool rescaled = false;
-        if (named_bar_or(1, 256, over)) {
+        if (named_bar_or(1, 256, !ok || dmax > 8.0f)) {
           if (named_bar_or(1, 256, !ok)) break;
           float mine = -INFINITY;
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
-            const float v = warp_max(x[h]);
+            const float v = warp_max(d[h]);
             if (lane == h) mine = v;
           }
           red[quad * 64 + 32 * hh + lane] = mine;
           named_bar_sync(2, 256);
           if (quad == 0) {  // one warp per head half moves the maxima
             const int hl = 32 * hh + lane;
-            const float mt = fmaxf(fmaxf(red[hl], red[64 + hl]), fmaxf(red[128 + hl], red[192 + hl]));
-            const float mo = m_run[hl];
-            const bool need = mt > mo + 8.0f;
-            al_own[hl] = need ? ex2_approx(mo - mt) : 1.0f;  // 0 while mo is -inf
-            if (need) m_run[hl] = mt;
+            const float dm = fmaxf(fmaxf(red[hl], red[64 + hl]), fmaxf(red[128 + hl], red[192 + hl]));
+            const bool need = dm > 8.0f;
+            al_own[hl] = need ? ex2_approx(-dm) : 1.0f;  // ~0 when the maximum was unset
+            if (need) m_run[hl] += dm;
           }
           named_bar_sync(2, 256);
+          // the scores again, against the new maxima (exact, where the step
+          // from an unset maximum was not)
+          load_d();
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 f = *reinterpret_cast<const float4*>(al_own + 32 * hh + h);
@@ -607,66 +677,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           rescaled = i > 0;  // O holds earlier tiles of this piece
         }
-        // P = 2^(x - m) as binary16 pairs, row sums per head
+        // the scores are read: the next tile's QK may overwrite them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_S_EMPTY));
+        // P = 2^d as binary16 pairs, row sums per head
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float2 mm = *reinterpret_cast<const float2*>(m_run + 32 * hh + 2 * k);
-          const float m0 = mm.x == -INFINITY ? 0.0f : mm.x;  // all masked so far: p = 0
-          const float m1 = mm.y == -INFINITY ? 0.0f : mm.y;
-          const float p0 = ex2_approx(x[2 * k] - m0);
-          const float p1 = ex2_approx(x[2 * k + 1] - m1);
+          const float p0 = ex2_approx(d[2 * k]);
+          const float p1 = ex2_approx(d[2 * k + 1]);
           l[2 * k] += p0;
           l[2 * k + 1] += p1;
           pk[k] = pack_half2(p0, p1);
         }
-        // The P buffer is free, and O holds the previous tile, once this
-        // CTA's P.V of tile t-1 has completed; the peer's copy of this CTA's
-        // rows is free once the peer's has.
+        // rescale packet for the peer's O rows of this CTA's heads: a flag
+        // and the factors, sent as soon as the decision is made
+        if (sw == 0 && lane <= 16) {
+          float4 f = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+          if (lane == 16)
+            f.x = rescaled ? 1.0f : 0.0f;
+          else if (rescaled)
+            f = *reinterpret_cast<const float4*>(al_own + 4 * lane);
+          st_async_v4(mapa(sb0 + kSmAlphaIn + (t & 1u) * kPkt + 16 * lane, peer), f.x, f.y, f.z, f.w,
+                      mapa(BAR(B_AX0 + (t & 1u)), peer));
+        }
+        // The P tile is free, and O holds the previous tile, once this CTA's
+        // P.V of tile t-1 has completed and the copy of its rows to the peer
+        // has read them.
         if (t > 0) {
           got = warp_ok(mbar_wait(BAR(B_PV_DONE), (t - 1) & 1u, abort_flag, kWaitNs));
-          if (got && lane == 0) mbar_arrive_remote(mapa(BAR(B_PFREE), peer));
-          got = got && warp_ok(mbar_wait<true>(BAR(B_PFREE), (t - 1) & 1u, abort_flag, kWaitNs));
+          got = got && warp_ok(mbar_wait(BAR(B_SRC_FREE), (t - 1) & 1u, abort_flag, kWaitNs));
           ok = ok && got;
         }
         if (!ok) continue;  // the next tile's barriers take every warp out together
         tc_fence_after();
-        if (rescaled && o_own) {
-          const float al = al_own[oh];
-          if (__any_sync(0xffffffffu, al != 1.0f)) rescale_o(al);
-        }
-        // P row tt of this CTA's heads into its atom here and in the peer
-        {
-          const uint32_t pbar = mapa(BAR(B_PX_FULL), peer);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t off = prow + uint32_t(((4 * hh + g) ^ (tt & 7)) << 4);
-            *reinterpret_cast<uint4*>(sm + off) =
-                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-            st_async_u32x4(mapa(sb0 + off, peer), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
-                           pk[4 * g + 3], pbar);
+        if (o_own) {
+          if (rescaled) {
+            const float al = al_own[oh];
+            if (__any_sync(0xffffffffu, al != 1.0f)) rescale_o(al);
           }
-          // rescale factors of this CTA's heads for the peer's O rows
-          if (sw == 0 && lane < 16) {
-            float4 f = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-            if (rescaled) f = *reinterpret_cast<const float4*>(al_own + 4 * lane);
-            st_async_v4(mapa(sb0 + kSmAlphaIn + 16 * lane, peer), f.x, f.y, f.z, f.w, pbar);
-          }
-        }
-        fence_proxy_async_smem();
-        if (!o_own) {
-          // the peer's rows and factors: rescale this CTA's O rows of the peer's heads
-          got = warp_ok(mbar_wait<true>(BAR(B_PX_FULL), t & 1u, abort_flag, kWaitNs));
+        } else {
+          // the peer's packet: rescale this CTA's O rows of the peer's heads
+          got = warp_ok(mbar_wait<true>(BAR(B_AX0 + (t & 1u)), (t >> 1) & 1u, abort_flag, kWaitNs));
           if (got) {
-            const float al = al_in[oh];
-            if (i > 0 && __any_sync(0xffffffffu, al != 1.0f)) rescale_o(al);
-            // the peer sends the next tile's exchange only after this tile's P.V
+            const float* pkt = reinterpret_cast<const float*>(sm + kSmAlphaIn + (t & 1u) * kPkt);
+            const float al = pkt[oh];
+            const bool flag = pkt[64] != 0.0f;
+            // the peer's packet two tiles ahead goes to this buffer
             if (hh == 0 && (quad & 1u) == 0 && lane == 0)
-              mbar_arrive_expect_tx(BAR(B_PX_FULL), kPx);
-            fence_proxy_async_smem();
+              mbar_arrive_expect_tx(BAR(B_AX0 + (t & 1u)), kPkt);
+            if (flag && i > 0 && __any_sync(0xffffffffu, al != 1.0f)) rescale_o(al);
           }
           ok = ok && got;
         }
+        // P row tt of this CTA's heads into its own P atom
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t off = prow + uint32_t(((4 * hh + g) ^ (tt & 7)) << 4);
+          *reinterpret_cast<uint4*>(sm + off) =
+              make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_P_LOCAL));
         tc_fence_before();
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(BAR(B_P_FULL));
@@ -732,7 +806,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant
-    // (keeps the launch's register count, kRegsDq)
+    setmaxnreg_inc<kRegsDq>();
     // thread = token row tt of the tile (tensor-memory lane); rows 0-63 come
     // from the tile's first block, 64-127 from its second.  Units per tile:
     //   dh 0: A (tensor memory) the other half's chunks 0, 1, 2;
@@ -747,29 +821,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t row_off = uint32_t(tt >> 3) * 1024u + uint32_t(tt & 7) * 128u;
     const int sw7 = tt & 7;
     const int qt = int(threadIdx.x) - kDqWarp0 * 32;  // 0..255
-    // block of this thread's row in tile i of piece s (nullptr: no such row,
-    // a bad block id, or a token past the sequence: read as zeros)
-    auto row_block = [&](int s, int i) -> const uint8_t* {
-      const int4 pc = a.ws.pieces[s];
-      const int j = pc.y + 2 * i + bi;
-      if (j >= pc.z) return nullptr;
-      const int32_t blk = a.block_table[int64_t(pc.x) * a.max_blocks_per_seq + j];
-      if (blk < 0 || blk >= a.num_blocks) {
-        if (lane == 0 && (dw == 0 || dw == 2)) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
-        return nullptr;
-      }
-      return slot < seq_len_clamped(a, pc.x) - j * kT ? a.blocks + int64_t(blk) * G.block : nullptr;
-    };
-    // the next tile of the worker after tile i of piece s (s > wr.y: none)
-    auto next_tile = [&](int& s, int& i) {
-      if (i + 1 < piece_tiles(a.ws.pieces[s])) {
-        ++i;
-        return;
-      }
-      i = 0;
-      for (++s; s <= wr.y && piece_tiles(a.ws.pieces[s]) == 0; ++s) {
-      }
-    };
     // this piece's queries (this CTA's 64 heads), binary16, SW128 K-major
     auto stage_q = [&](int b) {
       bool bad = false;
@@ -807,177 +858,188 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     unsigned char* ring = sm + kSmRing;
     uint32_t t = 0;
     bool ok = true;
-    int s = wr.x, i = 0;
-    while (s <= wr.y && piece_tiles(a.ws.pieces[s]) == 0) ++s;
-    if constexpr (!kBF16) {
-      // Packed codes: the A units of a tile are loaded while the previous
-      // tile's B units are processed, the B units (and the previous tile's
-      // late chunk) while its own A units are; each set has about one QK or
-      // P.V product's time to arrive, and only one set per phase is live.
-      Unit ua[3], ub[2];
-      int ps = -1, pi = 0;  // the previous tile (its late chunk goes to slot 3)
-      auto load_a = [&](int s2, int i2, uint32_t t2) {
-        const uint8_t* blk = row_block(s2, i2);
+    // this thread's row block in the previous tile (its late chunk goes to slot 3)
+    const uint8_t* prev_blk = nullptr;
+    // Packed codes: the A units of a tile are loaded while the previous tile's
+    // B units are processed, the B units (and the previous tile's late chunk)
+    // while its own A units are.  Block ids come 32 at a time from lane
+    // registers, so no code load waits for a block-table load.
+    // A units in processing order (pair k = 0, 1, 2), rotated down as they
+    // are consumed so that one copy of the unit code serves all three; B
+    // units: dh 0 two early chunks, dh 1 one early chunk and the previous
+    // tile's late chunk.  Each set is loaded as soon as the previous tile has
+    // consumed it, about a tile ahead of its use.
+    Unit ua0, ua1, ua2, ub0, ub1;
+    auto load_a = [&](const uint8_t* blk, uint32_t t2) {
+      if constexpr (!kBF16) {
         if (dh == 0) {
-#pragma unroll
-          for (int k = 0; k < 3; ++k) load_content<kCBits>(ua[k], blk, G, 4 * int(peer) + k, slot);
+          load_content<kCBits>(ua0, blk, G, 4 * int(peer) + 0, slot);
+          load_content<kCBits>(ua1, blk, G, 4 * int(peer) + 1, slot);
+          load_content<kCBits>(ua2, blk, G, 4 * int(peer) + 2, slot);
         } else {
-          load_content<kCBits>(ua[0], blk, G, 4 * int(peer) + 3, slot);
-          load_content<kCBits>(ua[1], blk, G, 4 * int(rank) + ((t2 & 1u) ? 0 : 3), slot);
-          load_rope(ua[2], blk, G, slot);
+          load_content<kCBits>(ua0, blk, G, 4 * int(peer) + 3, slot);
+          load_content<kCBits>(ua1, blk, G, 4 * int(rank) + ((t2 & 1u) ? 0 : 3), slot);
+          load_rope(ua2, blk, G, slot);
         }
+      }
+    };
+    for (int s = wr.x; ok && s <= wr.y; ++s) {
+      const int4 pc = a.ws.pieces[s];
+      const int nt = piece_tiles(pc);
+      if (nt == 0) continue;
+      const int L = seq_len_clamped(a, pc.x);
+      const int32_t* btab = a.block_table + int64_t(pc.x) * a.max_blocks_per_seq;
+      // block ids of blocks jb0 .. jb0+63 of the piece, one per lane in two registers
+      int jb0 = pc.y;
+      int32_t ids_a = (jb0 + lane < pc.z) ? btab[jb0 + lane] : -1;
+      int32_t ids_b = (jb0 + 32 + lane < pc.z) ? btab[jb0 + 32 + lane] : -1;
+      // block of this thread's row in tile i2 (nullptr: no such row, a bad
+      // block id, or a token past the sequence: read as zeros); called by the
+      // whole warp
+      auto tile_block = [&](int i2) -> const uint8_t* {
+        const int j = pc.y + 2 * i2 + bi, k = j - jb0;  // 0 <= k < 64
+        const int32_t va = __shfl_sync(0xffffffffu, ids_a, k & 31);
+        const int32_t vb = __shfl_sync(0xffffffffu, ids_b, k & 31);
+        if (j >= pc.z) return nullptr;
+        const int32_t blk = k < 32 ? va : vb;
+        if (blk < 0 || blk >= a.num_blocks) {
+          if (lane == 0 && (dw == 0 || dw == 2)) set_status(a.status, QMLA_STATUS_BAD_BLOCK);
+          return nullptr;
+        }
+        return slot < L - j * kT ? a.blocks + int64_t(blk) * G.block : nullptr;
       };
-      if (s <= wr.y) load_a(s, 0, 0);
-      while (ok && s <= wr.y) {
-        const int4 pc = a.ws.pieces[s];
-        bool got = t == 0 || mbar_wait(BAR(B_KT_EMPTY), (t - 1) & 1u, abort_flag, kWaitNs);
-        if (!warp_ok(got)) {
-          ok = false;
-          break;
-        }
-        if (i == 0) stage_q(pc.x);  // QK of the previous piece is complete
-        const uint32_t odd = t & 1u;
-        // ---- A: tensor-memory units
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const uint32_t u = dh == 0 ? uint32_t(k) : uint32_t(3 + k);
-          unit_to_tmem<kCBits>(ua[k], dh == 1 && k == 2, tbase + lane_base + kColK + 32u * u);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        // (the test hook withholds the first arrival of the first CTA of each pair)
-        if (lane == 0 && !(a.withhold && t == 0 && rank == 0)) mbar_arrive(BAR(B_KT_FULL));
-        // ---- the B units' codes, and the previous tile's late chunk (dh 1)
-        {
-          const uint8_t* blk = row_block(s, i);
+      const uint8_t* blk = tile_block(0);
+      load_a(blk, t);
+      auto load_b = [&](const uint8_t* b_blk, const uint8_t* c_blk, uint32_t t2) {
+        if constexpr (!kBF16) {
+          const uint32_t o2 = t2 & 1u;
           if (dh == 0) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              load_content<kCBits>(ub[k], blk, G, 4 * int(rank) + k + int(odd), slot);
+            load_content<kCBits>(ub0, b_blk, G, 4 * int(rank) + 0 + int(o2), slot);
+            load_content<kCBits>(ub1, b_blk, G, 4 * int(rank) + 1 + int(o2), slot);
           } else {
-            load_content<kCBits>(ub[0], blk, G, 4 * int(rank) + 2 + int(odd), slot);
-            load_content<kCBits>(ub[1], ps >= 0 ? row_block(ps, pi) : nullptr, G,
-                                 4 * int(rank) + (odd ? 3 : 0), slot);
+            load_content<kCBits>(ub0, b_blk, G, 4 * int(rank) + 2 + int(o2), slot);
+            // the late chunk of tile t2-1 (slot 3 after tile t2's B units)
+            load_content<kCBits>(ub1, c_blk, G, 4 * int(rank) + (o2 ? 3 : 0), slot);
           }
         }
-        // ---- B: this half's early chunks into the ring (slots of tile t-2)
-        got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
-        if (!warp_ok(got)) {
-          ok = false;
-          break;
+      };
+      load_b(blk, prev_blk, t);
+      const uint8_t* blk_next = nt > 1 ? tile_block(1) : nullptr;
+      for (int i = 0; i < nt; ++i, ++t) {
+        if (pc.y + 2 * i - jb0 >= 32) {  // slide the window (tile i+1 stays inside it)
+          jb0 += 32;
+          ids_a = ids_b;
+          ids_b = (jb0 + 32 + lane < pc.z) ? btab[jb0 + 32 + lane] : -1;
         }
-        const uint32_t base = odd ? 3u : 0u;
-        if (dh == 0) {
-          unit_to_ring<kCBits>(ub[0], ring + (base + odd) * kAtom, row_off, sw7);
-          unit_to_ring<kCBits>(ub[1], ring + (base + 1u + odd) * kAtom, row_off, sw7);
-        } else {
-          unit_to_ring<kCBits>(ub[0], ring + (base + 2u + odd) * kAtom, row_off, sw7);
+        if (i == 0) {
+          // this piece's queries, once every QK product of the previous piece is done
+          if (!warp_ok(t == 0 || mbar_wait(BAR(B_S_FULL), (t - 1) & 1u, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          stage_q(pc.x);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_RING_FULL));
-        // ---- the next tile's A codes
-        ps = s;
-        pi = i;
-        ++t;
-        next_tile(s, i);
-        if (s <= wr.y) load_a(s, i, t);
-        // ---- C: the previous tile's late chunk into slot 3 (freed with tile t-2's P.V)
-        if (dh == 1 && t >= 2) {
-          unit_to_ring<kCBits>(ub[1], ring + 3u * kAtom, row_off, sw7);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
-        }
-      }
-      // the last tile's late chunk
-      if (ok && dh == 1 && t >= 1) {
-        load_content<kCBits>(ub[1], row_block(ps, pi), G, 4 * int(rank) + (((t - 1) & 1u) ? 0 : 3),
-                             slot);
-        const bool got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
-        if (warp_ok(got)) {
-          unit_to_ring<kCBits>(ub[1], ring + 3u * kAtom, row_off, sw7);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
-        }
-      }
-    } else {
-      // BF16 rows: loaded, converted and stored unit by unit
-      int ps = -1, pi = 0;  // the previous tile (its late chunk goes to slot 3)
-      while (ok && s <= wr.y) {
-        const int4 pc = a.ws.pieces[s];
-        bool got = t == 0 || mbar_wait(BAR(B_KT_EMPTY), (t - 1) & 1u, abort_flag, kWaitNs);
-        if (!warp_ok(got)) {
-          ok = false;
-          break;
-        }
-        if (i == 0) stage_q(pc.x);
         const uint32_t odd = t & 1u;
-        const uint8_t* blk = row_block(s, i);
-        tc_fence_after();
+        const uint32_t base = odd ? 3u : 0u;
+        const uint32_t late_prev = odd ? 3u : 0u;  // the previous tile's late chunk
+        // ---- A: tensor-memory unit pairs, each once the previous tile's QK
+        // products on it are complete
 #pragma unroll 1
         for (int k = 0; k < 3; ++k) {
-          uint32_t v[32];
-          if (dh == 1 && k == 2)
-            load_bf16_rope(v, blk, G, slot);
-          else
-            load_bf16_content(v, blk, G,
-                              dh == 0 ? 4 * int(peer) + k
-                                      : (k == 0 ? 4 * int(peer) + 3 : 4 * int(rank) + (odd ? 0 : 3)),
-                              slot);
-          bf16_to_f16(v);
-          const uint32_t u = dh == 0 ? uint32_t(k) : uint32_t(3 + k);
-          tmem_st32(tbase + lane_base + kColK + 32u * u, v);
+          if (!warp_ok(t == 0 ||
+                       mbar_wait(BAR(B_KT_EMPTY + k), (t - 1) & 1u, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tbase + lane_base + kColK + 32u * uint32_t(dh == 0 ? k : 3 + k);
+          if constexpr (!kBF16) {
+            const Unit u = ua0;
+            ua0 = ua1;
+            ua1 = ua2;
+            unit_to_tmem<kCBits>(u, dh == 1 && k == 2, taddr);
+          } else {
+            uint32_t v[32];
+            if (dh == 1 && k == 2)
+              load_bf16_rope(v, blk, G, slot);
+            else
+              load_bf16_content(v, blk, G,
+                                dh == 0 ? 4 * int(peer) + k
+                                        : (k == 0 ? 4 * int(peer) + 3 : 4 * int(rank) + (odd ? 0 : 3)),
+                                slot);
+            bf16_to_f16(v);
+            tmem_st32(taddr, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          // (the test hook withholds the first arrival of the first CTA of each pair)
+          if (lane == 0 && !(a.withhold && t == 0 && rank == 0)) mbar_arrive(BAR(B_KT_FULL + k));
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_KT_FULL));
-        got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
-        if (!warp_ok(got)) {
+        if (!ok) break;
+        // ---- the next tile's A codes
+        if (i + 1 < nt) load_a(blk_next, t + 1);
+        // ---- B: this half's early chunks into the ring (slots of tile t-2)
+        if (!warp_ok(t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs))) {
           ok = false;
           break;
         }
-        const uint32_t base = odd ? 3u : 0u;
+        if constexpr (!kBF16) {
+          unit_to_ring<kCBits>(ub0, ring + (base + (dh == 0 ? 0u : 2u) + odd) * kAtom, row_off, sw7);
+          if (dh == 0) unit_to_ring<kCBits>(ub1, ring + (base + 1u + odd) * kAtom, row_off, sw7);
+        } else {
 #pragma unroll 1
-        for (int k = 0; k < (dh == 0 ? 2 : 1); ++k) {
-          const uint32_t c = (dh == 0 ? uint32_t(k) : 2u) + odd;
-          uint32_t v[32];
-          load_bf16_content(v, blk, G, 4 * int(rank) + int(c), slot);
-          bf16_to_f16(v);
-          st_row64(ring + (base + c) * kAtom, row_off, sw7, v);
+          for (int k = 0; k < (dh == 0 ? 2 : 1); ++k) {
+            const uint32_t c = (dh == 0 ? uint32_t(k) : 2u) + odd;
+            uint32_t v[32];
+            load_bf16_content(v, blk, G, 4 * int(rank) + int(c), slot);
+            bf16_to_f16(v);
+            st_row64(ring + (base + c) * kAtom, row_off, sw7, v);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_RING_FULL));
+        // ---- C: the previous tile's late chunk into slot 3 (freed with tile t-2's P.V)
         if (dh == 1 && t >= 1) {
-          uint32_t v[32];
-          load_bf16_content(v, row_block(ps, pi), G, 4 * int(rank) + ((t - 1) & 1u ? 0 : 3), slot);
-          bf16_to_f16(v);
-          st_row64(ring + 3u * kAtom, row_off, sw7, v);
+          if constexpr (!kBF16) {
+            unit_to_ring<kCBits>(ub1, ring + 3u * kAtom, row_off, sw7);
+          } else {
+            uint32_t v[32];
+            load_bf16_content(v, prev_blk, G, 4 * int(rank) + int(late_prev), slot);
+            bf16_to_f16(v);
+            st_row64(ring + 3u * kAtom, row_off, sw7, v);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
         }
-        ps = s;
-        pi = i;
-        ++t;
-        next_tile(s, i);
+        // ---- the next tile's B codes and this tile's late chunk
+        if (i + 1 < nt) load_b(blk_next, blk, t + 1);
+        prev_blk = blk;
+        blk = blk_next;
+        blk_next = i + 2 < nt ? tile_block(i + 2) : nullptr;
       }
-      if (ok && dh == 1 && t >= 1) {
-        const bool got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
-        if (warp_ok(got)) {
-          uint32_t v[32];
-          load_bf16_content(v, row_block(ps, pi), G, 4 * int(rank) + ((t - 1) & 1u ? 0 : 3), slot);
+    }
+    // the last tile's late chunk (tile t-1), once tile t-2's P.V has freed slot 3
+    if (ok && dh == 1 && t >= 1) {
+      const uint32_t lc = ((t - 1) & 1u) ? 0u : 3u;
+      uint32_t v[32];
+      if constexpr (!kBF16)
+        load_content<kCBits>(ub1, prev_blk, G, 4 * int(rank) + int(lc), slot);
+      else
+        load_bf16_content(v, prev_blk, G, 4 * int(rank) + int(lc), slot);
+      const bool got = t < 2 || mbar_wait(BAR(B_PV_DONE), t & 1u, abort_flag, kWaitNs);
+      if (warp_ok(got)) {
+        if constexpr (!kBF16) {
+          unit_to_ring<kCBits>(ub1, ring + 3u * kAtom, row_off, sw7);
+        } else {
           bf16_to_f16(v);
           st_row64(ring + 3u * kAtom, row_off, sw7, v);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_LATE_FULL));
       }
     }
   }

@@ -83,13 +83,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // raised by another thread, or `limit_ns` of wall time pass.  Returns false on
 // timeout or abort (the caller then unwinds).  On timeout it raises *abort so
 // every other role of the CTA unwinds too.
+// The abort flag and the clock are read once per 16 probes, so that a
+// waiting warp spends few instructions (and issue slots) per probe.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k)
+      if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
@@ -108,6 +112,24 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           "r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// This CTA's shared memory -> another CTA of the cluster (dst and the
+// destination's mbarrier `cluster_bar` as mapa addresses); completion counted
+// in bytes on that barrier.  16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2c(uint32_t dst, uint32_t src, uint32_t bytes,
+                                         uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "r"(src), "r"(bytes), "r"(cluster_bar)
+      : "memory");
+}
+// Close the bulk copies issued so far by this thread into a group, and wait
+// until every group's source bytes have been read (the sources may then be
+// overwritten; the destinations may still be in flight).
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Programmatic dependent launch: let the next kernel of the stream be
