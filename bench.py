@@ -2,20 +2,26 @@
 
 One step = append one new token to every sequence (quantize + pack) and run
 one decode over the whole cache (split-KV attention + log-sum-exp merge).
-Default workload: C4R4 cache, 32 sequences of 8192 tokens, 16 heads.
+Default workload (the headline): C4R4 cache, 4 sequences of 131072 tokens,
+128 heads (c4r4_b4_h128_l131072).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..4]
-                  [--format C4R4|C2R4|BF16] [--impl ours|reference] [--no-also]
+                  [--format C4R4|C2R4|BF16] [--impl ours|reference]
+                  [--cpu-procs P] [--no-also] [--no-footprint]
 
 Prints ONE JSON line on rank 0.  `value` is cached tokens attended per second
 (sum over the sequences of the tokens each decode attends, divided by the
 device time of the steps), aggregated over all ranks.  Inputs are synthetic
 and seeded (bit_mla_kv_qmla_gb300/workloads.py).  `--impl reference` times the
-CPU oracle on the host cores instead, on a bounded sample of the same
-workload.  Besides the contract's keys the line carries `roofline` (the
-decode call against the measured peaks), `cpu_baseline`, `e2e` (host
-buffers, copies inside the timed region), `footprint_150GB`, `capacity_sim`
-(the cache-pressure scheduler simulation) and, unless --no-also, `also`: the
+CPU oracle on the host cores instead (all of them by default, one process
+per core), on a bounded sample of the same workload.  Besides the contract's
+keys the line carries `roofline` (the decode call against the measured
+peaks, with the tensor-pipe activity ncu recorded for the same kernel
+sources), `cpu_baseline`, `e2e` (eager calls through the C ABI with host
+buffers, copies inside the timed region), `footprint_150GB` (the largest
+number of 131072-token sequences a 150 GB pool holds per format, and the
+decode rate measured at that concurrency), `capacity_sim` (the
+cache-pressure scheduler simulation) and, unless --no-also, `also`: the
 other workloads, the multi-token query decode, the folded-transform error
 and the RoPE-at-INT2 comparison.
 """
@@ -63,17 +69,46 @@ def decode_kernel_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name):
-    """DRAM bytes per decode launch from a committed ncu summary, if it was
-    taken on the current decode kernel sources; else None."""
+def recorded_profile(workload_name):
+    """The committed ncu figures of one decode launch of the workload's
+    dominant kernel (DRAM bytes, tensor-pipe activity), if they were taken on
+    the current decode kernel sources; else {}."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
-        return None
+        return {}
     d = json.load(open(p))
     ent = d.get(workload_name)
     if not ent or ent.get("kernel_hash") != decode_kernel_hash():
-        return None
-    return ent.get("traffic_bytes_per_launch")
+        return {}
+    return ent
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per decode launch from the committed ncu summary, or None."""
+    return recorded_profile(workload_name).get("traffic_bytes_per_launch")
+
+
+def host_cpu():
+    """Model name and logical core count of the host CPU."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    import platform
+    return {"model": model, "arch": platform.machine(), "logical_cores": os.cpu_count()}
 
 
 class ClockSampler:
@@ -164,6 +199,12 @@ def step_launches(w, n_app, tc):
     return k
 
 
+def append_per_step(cfg, w):
+    """Tokens appended per sequence per step: one for the serving steps
+    (configurations 1 and 4), the workload's own count otherwise."""
+    return max(1, w.n_append) if cfg in (1, 4) else w.n_append
+
+
 def run_ours(args, rank, world, device):
     import torch
     import bit_mla_kv_qmla_gb300 as q
@@ -172,7 +213,7 @@ def run_ours(args, rank, world, device):
 
     w = W.with_format(W.WORKLOADS[args.config], args.format or W.WORKLOADS[args.config].fmt)
     lens0 = W.seq_lens(w)
-    n_app = max(1, w.n_append) if args.config == 1 else w.n_append
+    n_app = append_per_step(args.config, w)
     total_steps = args.steps + args.warmup
     extra = n_app * (total_steps + 2 * args.e2e_steps + 4)
     cache_bytes = sum(W.blocks_needed(lens0, extra)) * q.qmla_block_bytes(w.fmt)
@@ -272,28 +313,39 @@ def run_ours(args, rank, world, device):
     for c in caches:
         assert c.status.item() == 0, "device status flag set during the benchmark"
 
-    # end to end through the public API with host buffers: per step, pinned
-    # host -> device copy of the step's inputs (new tokens, queries), the two
-    # library calls, device -> host read of O and LSE.
+    # End to end through the public API with host buffers, eager: per step,
+    # one pinned host -> device copy of that step's inputs (new tokens and
+    # queries, fresh for every step), the library calls issued through the C
+    # ABI (qmla_append_advance, qmla_decode: argument checks, ctypes
+    # marshalling and launches inside the timed region), and one device ->
+    # host read of O and LSE, then the host waits for it.
     e2e = None
     if args.e2e_steps > 0:
-        h_lat = new_lat[0, :, :max(n_app, 1)].cpu().pin_memory()
-        h_rope = new_rope[0, :, :max(n_app, 1)].cpu().pin_memory()
-        h_qc, h_qr = qc.cpu().pin_memory(), qr.cpu().pin_memory()
-        # the step's inputs in one pinned host buffer and one device buffer
-        # (one copy in), its outputs in the decoder's single out+lse buffer
-        # (one copy out); every region 256-byte aligned
-        srcs = [h_lat, h_rope, h_qc, h_qr] if n_app else [h_qc, h_qr]
+        n_sets = args.e2e_steps + 3
+        srcs_per = []
+        for k in range(n_sets):
+            qck, qrk = W.queries(w, step=k + 1)
+            lat = torch.stack([W.tokens(w, b, max(n_app, 1), offset_seed=10_000 + k)[0]
+                               for b in range(w.batch)])
+            rope = torch.stack([W.tokens(w, b, max(n_app, 1), offset_seed=10_000 + k)[1]
+                                for b in range(w.batch)])
+            srcs_per.append([lat, rope, qck, qrk] if n_app else [qck, qrk])
+        # every region 256-byte aligned, one pinned host buffer per step
         offs, off = [], 0
-        for t in srcs:
+        for t in srcs_per[0]:
             offs.append(off)
             off += (t.numel() * t.element_size() + 255) // 256 * 256
-        h_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+        h_ins = []
+        for srcs in srcs_per:
+            h = torch.empty(off, dtype=torch.uint8).pin_memory()
+            for t, o in zip(srcs, offs):
+                nb = t.numel() * t.element_size()
+                h[o:o + nb].copy_(t.contiguous().reshape(-1).view(torch.uint8))
+            h_ins.append(h)
         d_in = torch.empty(off, dtype=torch.uint8, device=device)
         views = []
-        for t, o in zip(srcs, offs):
+        for t, o in zip(srcs_per[0], offs):
             nb = t.numel() * t.element_size()
-            h_in[o:o + nb].copy_(t.reshape(-1).view(torch.uint8))
             views.append(d_in[o:o + nb].view(t.dtype).view(t.shape))
         if n_app:
             d_lat, d_rope, d_qc, d_qr = views
@@ -301,57 +353,45 @@ def run_ours(args, rank, world, device):
             d_qc, d_qr = views
             d_lat = d_rope = None
         h_io = torch.empty(decs[0].io.numel(), dtype=torch.uint8).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in srcs)
+        h2d = sum(t.numel() * t.element_size() for t in srcs_per[0])
         d2h = decs[0].out.numel() * 2 + decs[0].lse.numel() * 4
 
-        def e2e_calls(i):
-            d_in.copy_(h_in, non_blocking=True)
+        def e2e_step(k):
+            i = k % copies
+            d_in.copy_(h_ins[k], non_blocking=True)
             if n_app:
                 caches[i].append(d_lat[:, :n_app], d_rope[:, :n_app])
             decs[i](d_qc, d_qr, w.scale)
             h_io.copy_(decs[i].io, non_blocking=True)
-
-        def e2e_step(i):
-            e2e_calls(i)
-            torch.cuda.current_stream(device).synchronize()
-
-        if use_graph:
-            # The same calls captured once per cache copy (copies included)
-            # and replayed: a user who issues this step repeatedly does the
-            # same, and the host then waits for the result each step.
-            g_e2e = []
-            for i in range(copies):
-                ge = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(ge):
-                    e2e_calls(i)
-                g_e2e.append(ge)
-            torch.cuda.synchronize(device)
-
-            def e2e_step(i):  # noqa: F811
-                g_e2e[i].replay()
-                torch.cuda.current_stream(device).synchronize()
+            stream.synchronize()
 
         for k in range(3):
-            e2e_step(k % copies)
+            e2e_step(k)
             lens_at[k % copies] = [L + n_app for L in lens_at[k % copies]]
         tok_e2e = 0
         s0 = time.perf_counter()
-        for k in range(args.e2e_steps):
+        for k in range(3, n_sets):
+            e2e_step(k)
             i = k % copies
-            e2e_step(i)
             lens_at[i] = [L + n_app for L in lens_at[i]]
             tok_e2e += sum(lens_at[i])
         e2e_t = time.perf_counter() - s0
         e2e = {"value": tok_e2e / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_t / args.e2e_steps,
-               "issue": "CUDA graph replay" if use_graph else "eager calls"}
+               "issue": "eager C-ABI calls, fresh host inputs every step"}
 
     lens_mid = [L for L in lens_at[0]]
     pk = peaks()
-    roof = roofline_for(w.fmt, w.heads, lens_mid, t_dec, pk, recorded_traffic(w.name))
+    prof = recorded_profile(w.name)
+    roof = roofline_for(w.fmt, w.heads, lens_mid, t_dec, pk, prof.get("traffic_bytes_per_launch"))
     roof["decode_ms"] = round(t_dec * 1e3, 5)
-    tc = w.heads in (16, 128) and w.fmt in ("C4R4", "C2R4")
+    if prof.get("tensor_pipe_active_pct") is not None:
+        # ncu's sm__pipe_tensor_cycles_active of the same kernel sources (one
+        # launch, profiles/), next to the achieved fraction of the peak
+        roof["tensor_pipe_active_pct"] = prof["tensor_pipe_active_pct"]
+        roof["dram_throughput_pct"] = prof.get("dram_throughput_pct")
+    tc = w.heads in (16, 128) and w.fmt in ("C4R4", "C2R4", "BF16")
     roof["kernel"] = ((f"decode_tc{w.heads} (tcgen05"
                        + (", plans its own pieces)" if w.heads == 16 and w.batch <= 64
                           else ") + plan") + " + combine") if tc else
@@ -366,13 +406,17 @@ def run_ours(args, rank, world, device):
 
 
 def measure_also(args, device):
-    """Device-timed decode of the other workloads (no append), for context."""
+    """Device-timed decode of the other workloads and formats (decode only,
+    median of 10 calls with L2 flushed between them), for context."""
     import torch
     from bit_mla_kv_qmla_gb300 import workloads as W
     from bit_mla_kv_qmla_gb300.cache import Decoder, build_cache
     out = {}
     pk = peaks()
-    for cfg, fmt in [(1, "BF16"), (4, "C4R4"), (4, "C2R4"), (4, "BF16"), (2, "C4R4"), (3, "C2R4")]:
+    head = (args.config, args.format or W.WORKLOADS[args.config].fmt)
+    runs = [(1, "C4R4"), (1, "BF16"), (4, "C4R4"), (4, "C2R4"), (4, "BF16"), (2, "C4R4"),
+            (3, "C2R4")]
+    for cfg, fmt in [r for r in runs if r != head]:
         w = W.with_format(W.WORKLOADS[cfg], fmt)
         lens = W.seq_lens(w)
         cache = build_cache(w, device)
@@ -560,15 +604,76 @@ def measure_multi(device, pk):
     return {f"c4r4_b32_h16x{q_len}_l8192_multiquery": res}
 
 
-def footprint_sweep():
-    """Max concurrent L=131072 sequences in a 150 GB (1e9 B) cache budget."""
+def footprint_decode(device, budget=150e9, seq_len=131072, heads=128):
+    """The 150 GB footprint sweep, measured.  Per format: the largest number N
+    of seq_len-token sequences whose blocks fit the budget; a pool of exactly
+    those N x seq_len/64 blocks is filled from library-written blocks (one
+    sequence appended through qmla_append, its blocks then replicated with
+    device-to-device copies, one cudaMemcpyAsync per chunk of at most 4 GB),
+    and a 128-head decode over all N sequences is timed (median of 3, CUDA
+    events).  Reported: N, decode tokens/s (N sequences / step time) and
+    cached tokens attended/s.  If the device cannot hold the budget plus the
+    decode's buffers, the budget is lowered to what it can hold and stated."""
+    import torch
     import bit_mla_kv_qmla_gb300 as q
-    budget = 150e9
-    per_seq = {f: (131072 // 64) * q.qmla_block_bytes(f) for f in ("BF16", "C4R4", "C2R4")}
-    mx = {f: int(budget // per_seq[f]) for f in per_seq}
-    return {"budget_bytes": int(budget), "seq_len": 131072, "bytes_per_seq": per_seq,
-            "max_sequences": mx,
-            "gain_vs_bf16": {f: round(mx[f] / mx["BF16"], 3) for f in mx}}
+    from bit_mla_kv_qmla_gb300 import workloads as W
+    from bit_mla_kv_qmla_gb300.cache import Decoder, PagedCache
+    w4 = W.WORKLOADS[4]
+    nblk = seq_len // 64
+    free, total = torch.cuda.mem_get_info(device)
+    # decode buffers: queries, O and the split partials are a few GB at most
+    obtained = min(budget, free - 12e9)
+    per_seq = {f: nblk * q.qmla_block_bytes(f) for f in ("BF16", "C4R4", "C2R4")}
+    n_max = {f: int(budget // per_seq[f]) for f in per_seq}
+    res = {"budget_bytes": int(budget), "budget_obtained_bytes": int(obtained),
+           "seq_len": seq_len, "heads": heads, "bytes_per_seq": per_seq,
+           "max_sequences": n_max,
+           "gain_vs_bf16": {f: round(n_max[f] / n_max["BF16"], 3) for f in n_max},
+           "measured": {}}
+    for f in ("C4R4", "C2R4", "BF16"):
+        n = int(obtained // per_seq[f])
+        if n < 1:
+            continue
+        table = torch.arange(n * nblk, dtype=torch.int32).view(n, nblk)
+        cache = PagedCache(f, table, n * nblk, device)
+        lat, rope = W.tokens(w4, 0, seq_len, device=device)
+        cache.append_seq(0, lat, rope)
+        del lat, rope
+        seg = nblk * cache.block_bytes
+        chunk = max(1, int(4e9 // seg))
+        filled = 1
+        while filled < n:
+            k = min(filled, n - filled, chunk)
+            cache.blocks[filled * seg:(filled + k) * seg].copy_(cache.blocks[:k * seg])
+            filled += k
+        cache.seq_lens.fill_(seq_len)
+        g = torch.Generator(device=device)
+        g.manual_seed(4242)
+        qc = torch.randn(n, heads, W.D_C, generator=g, device=device).to(torch.bfloat16)
+        qr = torch.randn(n, heads, W.D_R, generator=g, device=device).to(torch.bfloat16)
+        dec = Decoder(cache, heads, seq_len)
+        for _ in range(2):
+            dec(qc, qr, w4.scale)
+        torch.cuda.synchronize(device)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(3)]
+        for a, b in evs:
+            a.record()
+            dec(qc, qr, w4.scale)
+            b.record()
+        torch.cuda.synchronize(device)
+        assert int(cache.status.item()) == 0, "device status flag set in the footprint decode"
+        t = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+        res["measured"][f] = {"sequences": n, "pool_bytes": n * seg, "decode_ms": round(t * 1e3, 3),
+                              "decode_tokens_per_s": round(n / t, 1),
+                              "tokens_attended_per_s": n * seq_len / t}
+        del cache, dec, qc, qr, table
+        torch.cuda.empty_cache()
+    m = res["measured"]
+    if "BF16" in m:
+        res["decode_tokens_per_s_vs_bf16"] = {
+            f: round(m[f]["decode_tokens_per_s"] / m["BF16"]["decode_tokens_per_s"], 3) for f in m}
+    return res
 
 
 def capacity_sweep(rates):
@@ -577,8 +682,9 @@ def capacity_sweep(rates):
     uniform in [8K, 128K] tokens and 1024 generated tokens each, at most 256
     running, cache budgets of 8, 16 and 32 GB.  Per format and budget:
     preemptions, tokens recomputed on readmission, decode steps and mean
-    running sequences; where this run measured the format's decode rate at 16
-    heads (tokens attended/s), the job's decode time at that rate."""
+    running sequences; and, where this run measured the format's decode rate
+    on the matching shape (128 heads, 131072-token sequences, the footprint
+    decode), the job's decode time at that rate (tokens attended / rate)."""
     import bit_mla_kv_qmla_gb300 as q
     from bit_mla_kv_qmla_gb300 import capacity as C
     reqs = C.synthetic_requests(512, 8192, 131072, 1024, seed=1)
@@ -594,7 +700,8 @@ def capacity_sweep(rates):
             row[f] = ent
         out[f"{gb}GB"] = row
     return {"requests": "512, prompts U[8192, 131072], 1024 generated, <= 256 running",
-            "rates_tokens_per_s": {f: round(v) for f, v in rates.items() if v},
+            "rates_tokens_attended_per_s": {f: round(v) for f, v in rates.items() if v},
+            "rate_shape": "128 heads, 131072-token sequences, decode at the 150 GB footprint",
             "by_budget": out}
 
 
@@ -604,16 +711,21 @@ def capacity_sweep(rates):
 
 class OracleRunner:
     """The oracle's step (append one token to each sampled sequence, then
-    decode them with every head), on the host, single-threaded."""
+    decode them) on the host, single-threaded, for sequences first ..
+    first+n_seq-1 and heads h0 .. h0+n_heads-1 of the workload.  A step's
+    tokens attended are counted in whole-decode units: the sampled
+    sequences' lengths times n_heads / heads (every head attends every
+    token, so a head subset is that fraction of the decode's work)."""
 
-    def __init__(self, cfg, fmt, n_seq, max_steps, first=0):
+    def __init__(self, cfg, fmt, n_seq, max_steps, first=0, h0=0, n_heads=None):
         import numpy as np
         import oracle
         from bit_mla_kv_qmla_gb300 import workloads as W
         self.np, self.oracle, self.W = np, oracle, W
         self.w = w = W.with_format(W.WORKLOADS[cfg], fmt)
         self.n_seq = n_seq
-        self.first = first  # sequences first .. first + n_seq - 1
+        self.first = first
+        self.n_heads = w.heads if n_heads is None else n_heads
         lens = W.seq_lens(w)[first:first + n_seq]
         self.f = W.FORMATS[w.fmt]
         need = [(L + max_steps + 1 + 63) // 64 for L in lens]
@@ -628,63 +740,91 @@ class OracleRunner:
             oracle.append(self.f, self.pool, self.table[b:b + 1], np.array([0], np.int32),
                           lat[None], rope[None])
         qc, qr = W.queries(w)
-        self.qc, self.qr = qc[first:first + n_seq], qr[first:first + n_seq]
+        hs = slice(h0, h0 + self.n_heads)
+        self.qc = qc[first:first + n_seq, hs].contiguous()
+        self.qr = qr[first:first + n_seq, hs].contiguous()
         self.cur = np.array(lens, np.int32)
         self.s = 0
-        self.sample = f"{n_seq} of {w.batch} sequences x {w.heads} heads per step"
+        self.sample = (f"{n_seq} of {w.batch} sequences x {self.n_heads} of {w.heads} heads "
+                       "per step")
 
     def step(self):
         self.s += 1
-        lat, rope = self.W.tokens(self.w, self.first, self.n_seq, offset_seed=self.s)
-        self.oracle.append(self.f, self.pool, self.table, self.cur, lat[:, None], rope[:, None])
+        # each sequence's appended token from its own stream, so that any
+        # split of the sequences over processes appends the same data
+        import torch
+        toks = [self.W.tokens(self.w, self.first + b, 1, offset_seed=self.s)
+                for b in range(self.n_seq)]
+        lat = torch.stack([t[0] for t in toks])
+        rope = torch.stack([t[1] for t in toks])
+        self.oracle.append(self.f, self.pool, self.table, self.cur, lat, rope)
         self.cur = self.cur + 1
         self.oracle.decode(self.f, self.pool, self.table, self.cur, self.qc, self.qr, self.w.scale)
-        return int(self.cur.sum())
+        return float(self.cur.sum()) * self.n_heads / self.w.heads
 
 
 def _oracle_worker(args):
-    """One process of the multi-core oracle timing: its own runner over a
-    disjoint set of sequences, timed between two barriers."""
+    """One process of the multi-core oracle timing: its own runner over its
+    own (sequences, heads) unit, timed between two barriers."""
     import torch
     torch.set_num_threads(1)  # one core per process (input generation included)
-    cfg, fmt, n_seq, first, steps, warmup, barrier = args
-    r = OracleRunner(cfg, fmt, n_seq, steps + warmup, first=first)
+    cfg, fmt, n_seq, first, h0, n_heads, steps, warmup, barrier = args
+    r = OracleRunner(cfg, fmt, n_seq, steps + warmup, first=first, h0=h0, n_heads=n_heads)
     for _ in range(warmup):
         r.step()
     barrier.wait()
-    tokens, t0 = 0, time.perf_counter()
+    tokens, t0 = 0.0, time.perf_counter()
     for _ in range(steps):
         tokens += r.step()
     return tokens, time.perf_counter() - t0
 
 
-def oracle_multicore(cfg, fmt, procs, n_seq, steps, warmup):
-    """The oracle's step over procs x n_seq sequences, split over procs
-    processes (started with spawn), all timed together.  Returns (tokens
-    attended / the slowest process's time, that time)."""
+def oracle_sample_shape(cfg):
+    """Per-process sample of the oracle timing: (sequences, heads).  Sized so
+    one step is about a second of single-core work."""
+    return {1: (2, 16), 2: (1, 32), 3: (1, 32), 4: (1, 8)}.get(cfg, (1, 16))
+
+
+def oracle_multicore(cfg, fmt, procs, steps, warmup):
+    """The oracle's step over procs disjoint (sequences, heads) units of the
+    workload, one process each (started with spawn), all timed together.
+    Returns (tokens attended / the slowest process's time, that time, the
+    units' description)."""
     import multiprocessing as mp
+    from bit_mla_kv_qmla_gb300 import workloads as W
+    w = W.WORKLOADS[cfg]
+    n_seq, n_heads = oracle_sample_shape(cfg)
+    units = [(b, h) for h in range(0, w.heads, n_heads) for b in range(0, w.batch, n_seq)]
+    procs = max(1, min(procs, len(units)))
+    jobs = [(cfg, fmt, n_seq, units[p][0], units[p][1], n_heads, steps, warmup)
+            for p in range(procs)]
     ctx = mp.get_context("spawn")
     with ctx.Manager() as mgr:
         barrier = mgr.Barrier(procs)
         with ctx.Pool(procs) as pool:
-            res = pool.map(_oracle_worker, [(cfg, fmt, n_seq, p * n_seq, steps, warmup, barrier)
-                                            for p in range(procs)])
+            res = pool.map(_oracle_worker, [j + (barrier,) for j in jobs])
     tokens = sum(r[0] for r in res)
     t = max(r[1] for r in res)
-    return tokens / t, t
+    desc = (f"{procs} processes, each {n_seq} of {w.batch} sequences x {n_heads} of {w.heads} "
+            "heads (disjoint units), tokens attended counted as that fraction of a decode")
+    return tokens / t, t, desc, procs
 
 
 def cpu_baseline(cfg, fmt):
-    """The oracle timed on a bounded sample (about 10 s of host work)."""
-    r = OracleRunner(cfg, fmt, n_seq=8 if cfg == 1 else 1, max_steps=64)
-    tokens, t0 = 0, time.perf_counter()
+    """The oracle timed on one core on a bounded sample (about 10 s of host
+    work after building the sample's cache)."""
+    n_seq, n_heads = {1: (8, 16), 4: (1, 16)}.get(cfg, (1, 16))
+    r = OracleRunner(cfg, fmt, n_seq=n_seq, max_steps=64, n_heads=n_heads)
+    tokens, t0 = 0.0, time.perf_counter()
     steps = 0
     while steps < 64 and (time.perf_counter() - t0 < 10.0 or steps < 1):
         tokens += r.step()
         steps += 1
     dt = time.perf_counter() - t0
     return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{r.sample}, {steps} step(s), {dt:.1f} s"}
+            "sample": (f"{r.sample}, {steps} step(s), {dt:.1f} s; tokens attended counted "
+                       f"as {n_heads}/{r.w.heads} of a decode per sequence"),
+            "cpu": host_cpu()}
 
 
 # ---------------------------------------------------------------------------
@@ -709,16 +849,18 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4])
     ap.add_argument("--format", default=None, choices=["C4R4", "C2R4", "BF16"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-procs", type=int, default=1,
-                    help="--impl reference: time the oracle in this many processes")
+    ap.add_argument("--cpu-procs", type=int, default=0,
+                    help="--impl reference: time the oracle in this many processes "
+                         "(0: one per host core)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--no-footprint", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
-                    help="launch each step's calls eagerly instead of replaying a CUDA graph")
+                    help="launch each timed step's calls eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -731,32 +873,18 @@ def main():
             return
         from bit_mla_kv_qmla_gb300 import workloads as W
         w = W.with_format(W.WORKLOADS[args.config], args.format or W.WORKLOADS[args.config].fmt)
-        n_seq = 2 if args.config == 1 else 1
-        procs = max(1, min(args.cpu_procs, w.batch // n_seq))
-        if procs == 1:
-            r = OracleRunner(args.config, w.fmt, n_seq=n_seq, max_steps=args.steps + args.warmup)
-            for _ in range(args.warmup):
-                r.step()
-            tokens, t0 = 0, time.perf_counter()
-            for _ in range(args.steps):
-                tokens += r.step()
-            t_all = time.perf_counter() - t0
-            v = tokens / t_all
-            sample = r.sample
-        else:
-            v, t_all = oracle_multicore(args.config, w.fmt, procs, n_seq, args.steps,
-                                        args.warmup)
-            sample = (f"{procs * n_seq} of {w.batch} sequences x {w.heads} heads per step, "
-                      f"{procs} processes of {n_seq}")
+        procs = args.cpu_procs if args.cpu_procs > 0 else (os.cpu_count() or 1)
+        v, t_all, sample, procs = oracle_multicore(args.config, w.fmt, procs, args.steps,
+                                                   args.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "format": w.fmt, "batch": w.batch,
                            "heads": w.heads, "seq_len": w.seq_len,
-                           "append_per_step": max(1, w.n_append)},
+                           "append_per_step": append_per_step(args.config, w)},
                 "cpu_baseline": {"value": v, "unit": UNIT, "cores": procs, "kind": "oracle",
-                                 "sample": sample},
+                                 "sample": sample, "cpu": host_cpu()},
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -778,15 +906,17 @@ def main():
             dist.destroy_process_group()
         return
     w = res["workload"]
+    torch.cuda.empty_cache()
     also = None if args.no_also or world > 1 else measure_also(args, device)
+    foot = None if args.no_footprint or world > 1 else footprint_decode(device)
+    rates = {f: m["tokens_attended_per_s"] for f, m in (foot or {}).get("measured", {}).items()}
     line = {
         "metric": METRIC, "value": tok / el, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": res["dtype"], "data": "synthetic (seeded, bit_mla_kv_qmla_gb300/workloads.py)",
         "config": {"workload": w.name, "format": w.fmt, "batch": w.batch, "heads": w.heads,
-                   "seq_len": w.seq_len,
-                   "append_per_step": max(1, w.n_append) if args.config == 1 else w.n_append,
+                   "seq_len": w.seq_len, "append_per_step": append_per_step(args.config, w),
                    "launch": ("CUDA graph replay of each step's library calls" if res["graph"]
                               else "eager library calls"),
                    "l2": (f"rotating {res['copies']} cache copies of "
@@ -797,10 +927,8 @@ def main():
         "e2e": res["e2e"],
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
-        "footprint_150GB": footprint_sweep(),
-        "capacity_sim": capacity_sweep({
-            "C4R4": tok / el if (w.fmt == "C4R4" and w.heads == 16) else None,
-            "BF16": (also or {}).get("bf16_b32_h16_l8192_append1", {}).get("tokens_per_s")}),
+        "footprint_150GB": foot,
+        "capacity_sim": capacity_sweep(rates),
         "also": also,
     }
     print(json.dumps(line))

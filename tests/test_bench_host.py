@@ -73,12 +73,29 @@ def test_capacity_sweep_shows_the_pressure_gap():
     assert "decode_s_at_measured_rate" not in at8["C2R4"]
 
 
-def test_oracle_multicore_covers_disjoint_sequences():
-    # two processes of two sequences each: the same tokens per step as one
-    # runner over four sequences (sequence b of the workload stays sequence b)
-    v, t = bench.oracle_multicore(1, "C4R4", 2, 2, steps=1, warmup=0)
-    assert v > 0 and t > 0
+def test_oracle_multicore_covers_disjoint_units():
+    # two processes, each its own (sequences, heads) unit of the workload
+    v, t, desc, procs = bench.oracle_multicore(1, "C4R4", 2, steps=1, warmup=0)
+    assert v > 0 and t > 0 and procs == 2 and "2 processes" in desc
+    # each sequence's appended tokens come from its own stream: splitting the
+    # sequences or the heads over runners appends the same bytes and counts
+    # the same work (head subsets as their fraction of the decode)
     one = bench.OracleRunner(1, "C4R4", 4, 1)
     two = [bench.OracleRunner(1, "C4R4", 2, 1, first=f) for f in (0, 2)]
-    assert one.step() == sum(r.step() for r in two)
+    halves = [bench.OracleRunner(1, "C4R4", 4, 1, h0=h, n_heads=8) for h in (0, 8)]
+    a = one.step()
+    assert a == sum(r.step() for r in two) == sum(r.step() for r in halves)
     assert (one.qc[2:] == two[1].qc).all()
+    assert (one.qc[:, 8:] == halves[1].qc).all()
+    bb = oracle.block_bytes(one.f)
+    for b, (r, rb) in enumerate([(two[0], 0), (two[0], 1), (two[1], 0), (two[1], 1)]):
+        for j in range(one.table.shape[1]):
+            x, y = one.table[b, j], r.table[rb, j]
+            if x < 0:
+                break
+            assert (one.pool[x * bb:(x + 1) * bb] == r.pool[y * bb:(y + 1) * bb]).all()
+
+
+def test_host_cpu_names_the_cores():
+    c = bench.host_cpu()
+    assert c["logical_cores"] == os.cpu_count() and c["arch"]
