@@ -52,3 +52,39 @@ def compare_rows(out, lse, ref_o, ref_l, label=""):
 def sample_heads(H: int, k: int, seed: int):
     g = torch.Generator().manual_seed(seed)
     return sorted(torch.randperm(H, generator=g)[:k].tolist())
+
+
+def plan_pieces(nblocks, workers: int, piece_cost: int):
+    """The decode's split plan, restated on the host: the blocks of all
+    sequences, each non-empty sequence preceded by piece_cost virtual blocks,
+    cut into min(workers, total) near-equal contiguous ranges.  Returns, per
+    sequence, its pieces as (worker, first block, end block)."""
+    ext = [n + piece_cost if n > 0 else 0 for n in nblocks]
+    N = sum(ext)
+    P = min(workers, N)
+    out, carry = [], 0
+    for n, e in zip(nblocks, ext):
+        pcs = []
+        if n > 0:
+            S = carry + piece_cost
+            first = ((S + 1) * P - 1) // N
+            last = ((S + n) * P - 1) // N
+            for wk in range(first, last + 1):
+                w0, w1 = wk * N // P, (wk + 1) * N // P
+                pcs.append((wk, max(w0 - S, 0), min(w1 - S, n)))
+        out.append(pcs)
+        carry += e
+    return out
+
+
+def boundary_sequences(nblocks, workers: int, piece_cost: int, k: int = 2):
+    """Sequences whose context a worker boundary cuts into the shortest
+    pieces (the split's most ragged merges): the k with the shortest partial
+    piece, then the one split over the most workers."""
+    plan = plan_pieces(nblocks, workers, piece_cost)
+    split = [(min(j1 - j0 for _, j0, j1 in p), b) for b, p in enumerate(plan) if len(p) > 1]
+    chosen = [b for _, b in sorted(split)[:k]]
+    most = max(range(len(plan)), key=lambda b: len(plan[b]))
+    if most not in chosen:
+        chosen.append(most)
+    return chosen

@@ -145,3 +145,27 @@ def test_decode_noalloc_rejects_bad_arguments(lib):
     # the formats qmla_decode serves are accepted up to the device query
     for fmt in (0, 1, 2, 3, 4):
         assert call(fmt=fmt, batch=0) == 0
+
+
+def test_host_plan_restatement_covers_every_block_once():
+    """The tests' host restatement of the split plan (used to pick the
+    full-size parity samples at worker boundaries): every block of every
+    sequence in exactly one piece, pieces in order, workers in order, and the
+    worker count capped by the total extent."""
+    import random
+    from helpers import boundary_sequences, plan_pieces
+    rng = random.Random(5)
+    for workers, cost in ((76, 2), (152, 3), (7, 0)):
+        nb = [rng.choice([0, 1, 2, 5, 64, 300]) for _ in range(50)]
+        plan = plan_pieces(nb, workers, cost)
+        seen = []
+        for b, pcs in enumerate(plan):
+            assert sum(j1 - j0 for _, j0, j1 in pcs) == nb[b]
+            pos = 0
+            for wk, j0, j1 in pcs:
+                assert j0 == pos and j1 > j0
+                pos = j1
+                seen.append(wk)
+        assert seen == sorted(seen) and max(seen) < min(workers, sum(n + cost for n in nb if n))
+        bs = boundary_sequences(nb, workers, cost)
+        assert all(len(plan[b]) > 1 for b in bs[:-1])

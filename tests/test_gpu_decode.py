@@ -13,7 +13,7 @@ from bit_mla_kv_qmla_gb300 import QMLA_STATUS_BAD_BLOCK, QMLA_STATUS_BAD_LEN
 from bit_mla_kv_qmla_gb300 import workloads as W
 from bit_mla_kv_qmla_gb300.cache import Decoder, PagedCache, build_cache
 
-from helpers import compare_rows, oracle_pool_for_seq, sample_heads
+from helpers import boundary_sequences, compare_rows, oracle_pool_for_seq, sample_heads
 
 pytestmark = pytest.mark.gpu
 FMTS = ["C4R4", "C2R4", "BF16", "C4R2", "C2R2"]
@@ -110,15 +110,22 @@ def test_decode_tiny_workload(fmt):
     compare_rows(out, lse, ref_o, ref_l, w.name)
 
 
-FULL = [(1, "C4R4", [0, 19], 6), (2, "C4R4", [3], 8), (3, "C2R4", [0, 40, 63], 6),
-        (4, "C4R4", [1], 8), (4, "C2R4", [2], 6), (4, "BF16", [0], 6), (1, "BF16", [5, 30], 16),
-        (1, "C2R2", [4], 8), (2, "C4R2", [11], 6), (2, "C2R4", [7], 6), (3, "C4R4", [20, 51], 6)]
+# seqs None: the sequences of the 128-head split plan whose context a worker
+# boundary cuts into the shortest pieces, and the one split the most
+FULL = [(1, "C4R4", [0, 19], 6), (2, "C4R4", [3], 8), (3, "C2R4", None, 6),
+        (4, "C4R4", None, 8), (4, "C2R4", None, 6), (4, "BF16", [0], 6), (1, "BF16", [5, 30], 16),
+        (1, "C2R2", [4], 8), (2, "C4R2", [11], 6), (2, "C2R4", [7], 6), (3, "C4R4", None, 6)]
 
 
 @pytest.mark.parametrize("cfg,fmt,seqs,nheads", FULL)
 def test_decode_full_size_sampled(cfg, fmt, seqs, nheads):
     w = W.with_format(W.WORKLOADS[cfg], fmt)
     lens = W.seq_lens(w)
+    if seqs is None:
+        assert w.heads == 128
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        # the 128-head kernel: one worker per CTA pair, two blocks of piece cost
+        seqs = boundary_sequences([(L + 63) // 64 for L in lens], sms // 2, 2)
     cache = build_cache(w, "cuda", gen_device="cuda")
     qc, qr = W.queries(w, device="cuda")
     out, lse = Decoder(cache, w.heads, max(lens))(qc, qr, w.scale)
@@ -282,3 +289,32 @@ def test_decode_max_heads():
     ref_o, ref_l = _oracle_full(w, cache, lens, qc, qr, "cpu")
     hs = sample_heads(256, 24, 5)
     compare_rows(out[:, hs], lse[:, hs], ref_o[:, hs], ref_l[:, hs], "H256")
+
+
+def test_plan_matches_host_restatement():
+    """The planner kernel's pieces (read back from the decode's workspace)
+    equal the tests' host restatement of the split, on the varied-length
+    128-head workload, so the full-size samples drawn from that restatement
+    sit at real worker boundaries."""
+    from helpers import plan_pieces
+    w = W.WORKLOADS[3]
+    lens = W.seq_lens(w)
+    cache = build_cache(w, "cuda", gen_device="cuda")
+    qc, qr = W.queries(w, device="cuda")
+    dec = Decoder(cache, w.heads, max(lens))
+    dec(qc, qr, w.scale)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H = w.batch, w.heads
+    slots = B + 2 * sms  # batch + the larger of the decode kernels' worker counts
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    ws = dec.workspace.cpu()
+    seq_table = ws[:B * 8].view(torch.int32).view(B, 2)
+    off = a256(B * 8) + a256(slots * H * 4) + a256(slots * H * 512 * 4)
+    pieces = ws[off:off + slots * 16].view(torch.int32).view(slots, 4)
+    want = plan_pieces([(L + 63) // 64 for L in lens], sms // 2, 2)
+    for b in range(B):
+        base, n = seq_table[b].tolist()
+        assert n == len(want[b]), b
+        for i, (_, j0, j1) in enumerate(want[b]):
+            assert pieces[base + i].tolist() == [b, j0, j1, 0], (b, i)
