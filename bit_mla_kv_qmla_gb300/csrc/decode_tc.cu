@@ -433,9 +433,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t vbase = (pt & 1u) ? 3u * kAtom : 0u;
 #pragma unroll
-      for (uint32_t kt = 0; kt < 8; ++kt)
-        mma_ss_warp(tbase + kColO, dP + ((kt * 2048u) >> 4), dV + ((vbase + kt * 2048u) >> 4), idp,
-                    (pfirst && kt == 0) ? 0u : 1u);
+      for (uint32_t kt = 0; kt < 8; kt += 4)
+        mma_ss_warp_x4(tbase + kColO, dP + ((kt * 2048u) >> 4), dV + ((vbase + kt * 2048u) >> 4),
+                       idp, (pfirst && kt == 0) ? 0u : 1u, 2048u >> 4, 2048u >> 4);
       mma_commit_warp(BAR(B_PV_DONE));
       return true;
     };
@@ -469,10 +469,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (uint32_t h = 0; h < 2; ++h) {
             const uint32_t u = k + 3u * h;
             const uint32_t qc = u < 4 ? 4u * peer + u : (u == 4 ? 4u * rank + lc : 8u);
-#pragma unroll
-            for (uint32_t ks = 0; ks < 4; ++ks)
-              mma_ts_warp(tbase + kColS, tbase + kColK + 32u * u + 8u * ks,
-                          dQ + ((qc * kQChunk + 32u * ks) >> 4), idq, (u | ks) ? 1u : 0u);
+            mma_ts_warp_x4(tbase + kColS, tbase + kColK + 32u * u, dQ + ((qc * kQChunk) >> 4), idq,
+                           u ? 1u : 0u, 8u, 32u >> 4);
           }
           mma_commit_warp(BAR(B_KT_EMPTY + k));
         }
@@ -487,10 +485,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (uint32_t e = 0; e < 3; ++e) {
           const uint32_t c = e + odd;
-#pragma unroll
-          for (uint32_t ks = 0; ks < 4; ++ks)
-            mma_ss_warp(tbase + kColS, dK + (((base + c) * kAtom + 32u * ks) >> 4),
-                        dQ + (((4u * rank + c) * kQChunk + 32u * ks) >> 4), idq, 1u);
+          mma_ss_warp_x4(tbase + kColS, dK + (((base + c) * kAtom) >> 4),
+                         dQ + (((4u * rank + c) * kQChunk) >> 4), idq, 1u, 32u >> 4, 32u >> 4);
         }
         mma_commit_warp(BAR(B_S_FULL));
         if (pend && !issue_pv()) {

@@ -345,6 +345,46 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four MMAs of consecutive K steps from one elected lane of a converged
+// warp, one election for all four: A advances a_step (tensor-memory columns
+// for the ts form, 16-byte descriptor units for the ss form), B b_step
+// descriptor units per step; only the first MMA may overwrite D
+// (accumulate0 = 0).
+__device__ __forceinline__ void mma_ts_warp_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate0,
+                                               uint32_t a_step, uint32_t b_step) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, e;\n\t.reg .b32 r, a1, a2, a3;\n\t.reg .b64 sb, b1, b2, b3;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+      "add.u32 a1, %1, %5;\n\tadd.u32 a2, a1, %5;\n\tadd.u32 a3, a2, %5;\n\t"
+      "cvt.u64.u32 sb, %6;\n\t"
+      "add.u64 b1, %2, sb;\n\tadd.u64 b2, b1, sb;\n\tadd.u64 b3, b2, sb;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate0), "r"(a_step), "r"(b_step)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_warp_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate0,
+                                               uint32_t a_step, uint32_t b_step) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, e;\n\t.reg .b32 r;\n\t"
+      ".reg .b64 sa, sb, a1, a2, a3, b1, b2, b3;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+      "cvt.u64.u32 sa, %5;\n\tcvt.u64.u32 sb, %6;\n\t"
+      "add.u64 a1, %1, sa;\n\tadd.u64 a2, a1, sa;\n\tadd.u64 a3, a2, sa;\n\t"
+      "add.u64 b1, %2, sb;\n\tadd.u64 b2, b1, sb;\n\tadd.u64 b3, b2, sb;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate0), "r"(a_step), "r"(b_step)
+      : "memory");
+}
 // Arrive once on `bar` when every tcgen05.mma issued so far by the elected
 // lane has completed.  The elected lane is the lowest active one, the same
 // lane for every call of a converged warp, so the commit tracks that lane's
