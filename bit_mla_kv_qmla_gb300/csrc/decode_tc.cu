@@ -71,6 +71,11 @@ namespace tc {
 // and the slot range of each worker.
 __global__ void __launch_bounds__(32) plan_kernel(DecodeArgs a) {
   const int lane = threadIdx.x;
+  // Launched as a programmatic dependent of the kernel before it (the append
+  // that advances seq_lens, say): the decode after it may be scheduled now,
+  // and nothing is read before that kernel has completed.
+  if (lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t N = plan_total(a);
   const int64_t P = plan_workers(N, a.workers);
   // a worker that owns only piece-cost blocks (or none) has no piece
@@ -113,8 +118,17 @@ __global__ void __launch_bounds__(32) plan_kernel(DecodeArgs a) {
 
 // The planner kernel is defined once, here, for both tensor-core decodes.
 cudaError_t launch_plan(const DecodeArgs& a, cudaStream_t stream) {
-  tc::plan_kernel<<<1, 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc::plan_kernel, a);
 }
 
 namespace {
@@ -397,6 +411,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers are initialized before any remote arrive
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kSmTslot);
+  // The kernel is launched as a programmatic dependent of the planner: the
+  // set-up above overlaps it, and no thread reads global memory before the
+  // planner (and, through its own wait, the kernel before it) has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the merge kernel that follows may be scheduled now (it waits for this
+  // grid to complete before it reads anything)
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int2 wr = a.ws.wrange[pair];
 
   if (warp < kSmxWarp0) {
@@ -1075,8 +1096,17 @@ cudaError_t launch_decode_tc128(const DecodeArgs& a, cudaStream_t stream) {
   e = ensure_smem_attr(kernel, int(kSmDyn),
                        a.fmt == QMLA_C4R4 ? done4 : a.fmt == QMLA_C2R4 ? done2 : done16);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3(unsigned(2 * a.workers)), kThreads, kSmDyn, stream>>>(b);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(2 * a.workers));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmDyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, b);
 }
 
 int tc_workers(int sms, int heads) {
