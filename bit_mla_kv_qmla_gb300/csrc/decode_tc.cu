@@ -52,7 +52,8 @@
 // runs faster with 64).  Binary16 operands (exact on the quantizer's grid),
 // binary32 accumulation.  The softmax is online in base 2 with lazy
 // rescaling: the running maximum of a head only moves when a score exceeds
-// it by more than 8 (P <= 256).  Every
+// it by more than kLazy = 15 (P < 2^15, inside binary16's range; row sums
+// and O are binary32).  Every
 // wait is bounded in time; on timeout the CTA raises an abort flag, all
 // roles unwind and QMLA_STATUS_TIMEOUT is reported.
 //
@@ -199,6 +200,11 @@ constexpr uint32_t kPx = 128 * 64 * 2;  // P rows of one CTA's heads per tile
 // that scores minus it stay exact enough to find the first maximum, and far
 // below any score of binary16 operands that the softmax can represent.
 constexpr float kMaxUnset = -32768.0f;
+// Lazy rescaling: a head's running maximum moves only when a score exceeds it
+// by more than this (log2 units).  P = 2^d then stays below 2^15, exact in
+// binary16's range; a smaller margin rescales far more often on coarse (INT2)
+// keys, whose scores spread more.
+constexpr float kLazy = 15.0f;
 static_assert(kSmP % 1024 == 0 && kSmRing % 1024 == 0, "SW128 operand tiles are 1 KB aligned");
 static_assert(kSmBar % 8 == 0, "mbarrier alignment");
 static_assert(kSmDyn <= 232448, "shared memory budget");
@@ -656,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ok = ok && got;
         // lazy rescale: a head's maximum only moves when one of its scores
-        // exceeds it by more than 8 (an unset maximum is kMaxUnset, below any
+        // exceeds it by more than kLazy (an unset maximum is kMaxUnset, below any
         // score); the decisions are the same in every thread.  All eight
         // warps take every barrier below whatever their waits returned: a
         // failed wait forces the rare path, which leaves the loop together.
@@ -664,7 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 1; h < 32; ++h) dmax = fmaxf(dmax, d[h]);
         bool rescaled = false;
-        if (named_bar_or(1, 256, !ok || dmax > 8.0f)) {
+        if (named_bar_or(1, 256, !ok || dmax > kLazy)) {
           if (named_bar_or(1, 256, !ok)) break;
           float mine = -INFINITY;
 #pragma unroll
@@ -677,7 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (quad == 0) {  // one warp per head half moves the maxima
             const int hl = 32 * hh + lane;
             const float dm = fmaxf(fmaxf(red[hl], red[64 + hl]), fmaxf(red[128 + hl], red[192 + hl]));
-            const bool need = dm > 8.0f;
+            const bool need = dm > kLazy;
             al_own[hl] = need ? ex2_approx(-dm) : 1.0f;  // ~0 when the maximum was unset
             if (need) m_run[hl] += dm;
           }

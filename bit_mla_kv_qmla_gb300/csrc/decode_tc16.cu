@@ -31,9 +31,10 @@
 //
 // The softmax runs over tokens, i.e. across the 128 lanes of S^T.  A tile
 // first checks, with one OR-barrier, whether any score exceeds the running
-// maximum by more than 8 (log2 units); only then are per-head maxima reduced
-// and O^T rescaled (lazy rescaling).  Row sums are kept per lane and reduced
-// once per piece.
+// maximum by more than kLazy = 15 (log2 units; P < 2^15 stays inside
+// binary16's range, row sums and O are binary32); only then are per-head
+// maxima reduced and O^T rescaled (lazy rescaling).  Row sums are kept per
+// lane and reduced once per piece.
 //
 // Warp roles (14 warps): 0 QK issuer, 1 P.V issuer, 2-5 softmax (thread =
 // token lane), 6-13 dequantization (two warps per lane quarter).  Binary16 operands (exact on the quantizer's grid), binary32
@@ -56,6 +57,8 @@ constexpr int kPvWarp = 1;
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kDequantWarp0 = 6;
 constexpr int kH = 16;  // heads
+// lazy-rescale margin (log2 units): P = 2^(s - m) < 2^15
+constexpr float kLazy = 15.0f;
 
 // tensor memory columns (32-bit); K holds binary16 pairs (channel 2j, 2j+1)
 constexpr uint32_t kTmemCols = 512;
@@ -465,13 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
           }
         }
         // lazy rescale: the per-head maxima are only reduced when some score
-        // exceeds the maximum in use by more than 8; every thread then takes
+        // exceeds the maximum in use by more than kLazy; every thread then takes
         // the same decisions.  All four warps take the same barriers whatever
         // their waits returned: a failed wait forces the rare path, which
         // checks for it.
         bool over = !got;
 #pragma unroll
-        for (int h = 0; h < kH; ++h) over |= sv[h] > m_used[h] + 8.0f;
+        for (int h = 0; h < kH; ++h) over |= sv[h] > m_used[h] + kLazy;
         if (named_bar_or(1, 128, over)) {
           if (named_bar_or(1, 128, !got)) {
             ok = false;
@@ -500,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc16_kernel(DecodeArgs a) 
                                  fmaxf(fmaxf(v0.w, v1.w), fmaxf(v2.w, v3.w))};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const bool need = mt[e] > m_used[h + e] + 8.0f;
+              const bool need = mt[e] > m_used[h + e] + kLazy;
               alpha[h + e] = need ? ex2_approx(m_used[h + e] - mt[e]) : 1.0f;
               if (need) m_used[h + e] = mt[e];
             }
