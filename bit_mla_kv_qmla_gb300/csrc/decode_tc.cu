@@ -46,11 +46,12 @@
 // idle); 4-11 softmax (thread = token row of S^T; two warps per
 // tensor-memory lane quarter, 32 heads each); 12-19 dequantization (thread =
 // token row; two warps per lane quarter).  The first warpgroup hands part of
-// its registers to the other four (setmaxnreg): 64 + 104 (softmax) + 104
+// its registers to the other four (setmaxnreg): 48 + 104 (softmax) + 112
 // (dequantization) per thread of each sub-partition's five warps, within the
-// launch's 96 x 5 (measured best of the splits that fit; the issuer's loop
-// runs faster with 64).  Binary16 operands (exact on the quantizer's grid),
-// binary32 accumulation.  The softmax is online in base 2 with lazy
+// launch's 96 x 5, for the low-bit formats (the dequantization warps hold a
+// tile's packed codes a tile ahead of use), 64 + 104 + 104 for BF16 rows
+// (measured best of the splits that fit).  Binary16 operands (exact on the
+// quantizer's grid), binary32 accumulation.  The softmax is online in base 2 with lazy
 // rescaling: the running maximum of a head only moves when a score exceeds
 // it by more than kLazy = 15 (P < 2^15, inside binary16's range; row sums
 // and O are binary32).  Every
@@ -143,9 +144,14 @@ constexpr int kMmaWarp = 0;
 constexpr int kXchgWarp = 1;   // moves this CTA's P rows to the peer
 constexpr int kSmxWarp0 = 4;   // 8 softmax warps (warpgroups 1-2)
 constexpr int kDqWarp0 = 12;   // 8 dequantization warps (warpgroups 3-4)
-constexpr uint32_t kRegsIdle = 64, kRegsSmx = 104, kRegsDq = 104;
-static_assert(128 * kRegsIdle + 256 * kRegsSmx + 256 * kRegsDq <= kThreads * 96,
-              "register split within the launch allocation (96 per thread at 20 warps)");
+// registers per thread of the issuer warpgroup, the softmax and the
+// dequantization warps; the BF16 rows need no codes held ahead of use
+template <int kCBits>
+struct RegSplit {
+  static constexpr uint32_t idle = kCBits == 16 ? 64 : 48, smx = 104, dq = kCBits == 16 ? 104 : 112;
+  static_assert(128 * idle + 256 * smx + 256 * dq <= kThreads * 96,
+                "register split within the launch allocation (96 per thread at 20 warps)");
+};
 
 // tensor memory (32-bit columns)
 constexpr uint32_t kTmemCols = 512;
@@ -429,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp < kSmxWarp0) {
     // the first warpgroup (all four warps at this one instruction) gives up
     // registers; only its first warp has work
-    setmaxnreg_dec<kRegsIdle>();
+    setmaxnreg_dec<RegSplit<kCBits>::idle>();
   }
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -569,7 +575,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // idle warps of the first warpgroup
   } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ softmax
-    setmaxnreg_inc<kRegsSmx>();
+    setmaxnreg_inc<RegSplit<kCBits>::smx>();
     // thread = token row tt of S^T (its lane quarter's tensor-memory lanes);
     // the warp holds 32 of this CTA's 64 heads.  For O (lane = head) the same
     // thread stands for head tt.
@@ -830,7 +836,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant
-    setmaxnreg_inc<kRegsDq>();
+    setmaxnreg_inc<RegSplit<kCBits>::dq>();
     // thread = token row tt of the tile (tensor-memory lane); rows 0-63 come
     // from the tile's first block, 64-127 from its second.  Units per tile:
     //   dh 0: A (tensor memory) the other half's chunks 0, 1, 2;
