@@ -17,8 +17,9 @@ CPU oracle on the host cores instead (all of them by default, one process
 per core), on a bounded sample of the same workload.  Besides the contract's
 keys the line carries `roofline` (the decode call against the measured
 peaks, with the tensor-pipe activity ncu recorded for the same kernel
-sources), `cpu_baseline`, `e2e` (eager calls through the C ABI with host
-buffers, copies inside the timed region), `footprint_150GB` (the largest
+sources), `cpu_baseline`, `e2e` (one qmla_decode_step call per step through
+the C ABI, host buffers in and out, copies inside the timed region),
+`footprint_150GB` (the largest
 number of 131072-token sequences a 150 GB pool holds per format, and the
 decode rate measured at that concurrency), `capacity_sim` (the
 cache-pressure scheduler simulation) and, unless --no-also, `also`: the
@@ -313,57 +314,44 @@ def run_ours(args, rank, world, device):
     for c in caches:
         assert c.status.item() == 0, "device status flag set during the benchmark"
 
-    # End to end through the public API with host buffers, eager: per step,
-    # one pinned host -> device copy of that step's inputs (new tokens and
-    # queries, fresh for every step), the library calls issued through the C
-    # ABI (qmla_append_advance, qmla_decode: argument checks, ctypes
-    # marshalling and launches inside the timed region), and one device ->
-    # host read of O and LSE, then the host waits for it.
+    # End to end through the public API with host buffers: per step one call
+    # of qmla_decode_step (C ABI) from a page-locked host buffer holding that
+    # step's inputs (new tokens and queries, different for every step) to a
+    # page-locked host buffer receiving O and LSE: inside the call one host ->
+    # device copy, the append and length update, the decode (planner, decode,
+    # merge), one device -> host copy, and the wait for it.
     e2e = None
     if args.e2e_steps > 0:
         n_sets = args.e2e_steps + 3
-        srcs_per = []
+        lay = q.qmla_decode_step_layout(w.batch, w.heads, n_app)
+        h_ins = []
         for k in range(n_sets):
             qck, qrk = W.queries(w, step=k + 1)
-            lat = torch.stack([W.tokens(w, b, max(n_app, 1), offset_seed=10_000 + k)[0]
-                               for b in range(w.batch)])
-            rope = torch.stack([W.tokens(w, b, max(n_app, 1), offset_seed=10_000 + k)[1]
-                                for b in range(w.batch)])
-            srcs_per.append([lat, rope, qck, qrk] if n_app else [qck, qrk])
-        # every region 256-byte aligned, one pinned host buffer per step
-        offs, off = [], 0
-        for t in srcs_per[0]:
-            offs.append(off)
-            off += (t.numel() * t.element_size() + 255) // 256 * 256
-        h_ins = []
-        for srcs in srcs_per:
-            h = torch.empty(off, dtype=torch.uint8).pin_memory()
-            for t, o in zip(srcs, offs):
-                nb = t.numel() * t.element_size()
-                h[o:o + nb].copy_(t.contiguous().reshape(-1).view(torch.uint8))
+            srcs = [(lay[2], qck), (lay[3], qrk)]
+            if n_app:
+                lat = torch.stack([W.tokens(w, b, n_app, offset_seed=10_000 + k)[0]
+                                   for b in range(w.batch)])
+                rope = torch.stack([W.tokens(w, b, n_app, offset_seed=10_000 + k)[1]
+                                    for b in range(w.batch)])
+                srcs = [(lay[0], lat), (lay[1], rope)] + srcs
+            h = torch.zeros(lay[4], dtype=torch.uint8).pin_memory()
+            for o, t in srcs:
+                raw = t.contiguous().reshape(-1).view(torch.uint8)
+                h[o:o + raw.numel()].copy_(raw)
             h_ins.append(h)
-        d_in = torch.empty(off, dtype=torch.uint8, device=device)
-        views = []
-        for t, o in zip(srcs_per[0], offs):
-            nb = t.numel() * t.element_size()
-            views.append(d_in[o:o + nb].view(t.dtype).view(t.shape))
-        if n_app:
-            d_lat, d_rope, d_qc, d_qr = views
-        else:
-            d_qc, d_qr = views
-            d_lat = d_rope = None
-        h_io = torch.empty(decs[0].io.numel(), dtype=torch.uint8).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in srcs_per[0])
-        d2h = decs[0].out.numel() * 2 + decs[0].lse.numel() * 4
+        h_out = torch.empty(lay[7], dtype=torch.uint8).pin_memory()
+        ws_step = [torch.empty(q.qmla_decode_step_workspace_bytes(w.fmt, w.batch, w.heads, n_app,
+                                                                  d.max_seq_len),
+                               dtype=torch.uint8, device=device) for d in decs]
+        h2d = lay[4]
+        d2h = lay[7]
 
         def e2e_step(k):
             i = k % copies
-            d_in.copy_(h_ins[k], non_blocking=True)
-            if n_app:
-                caches[i].append(d_lat[:, :n_app], d_rope[:, :n_app])
-            decs[i](d_qc, d_qr, w.scale)
-            h_io.copy_(decs[i].io, non_blocking=True)
-            stream.synchronize()
+            c = caches[i]
+            q.qmla_decode_step(w.fmt, c.blocks, c.block_table, c.seq_lens, decs[i].max_seq_len,
+                               w.heads, n_app, h_ins[k], w.scale, h_out, ws_step[i], c.status,
+                               stream)
 
         for k in range(3):
             e2e_step(k)
@@ -379,7 +367,8 @@ def run_ours(args, rank, world, device):
         e2e = {"value": tok_e2e / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_t / args.e2e_steps,
-               "issue": "eager C-ABI calls, fresh host inputs every step"}
+               "issue": "one qmla_decode_step call per step: page-locked host buffers in and "
+                        "out, fresh inputs every step"}
 
     lens_mid = [L for L in lens_at[0]]
     pk = peaks()

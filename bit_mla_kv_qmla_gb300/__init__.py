@@ -7,6 +7,8 @@ returned by the library raise QmlaError.
 """
 from __future__ import annotations
 
+import functools
+
 from typing import Optional
 
 from . import _lib
@@ -47,6 +49,7 @@ def _check(fn: str, code: int) -> None:
         raise QmlaError(fn, code)
 
 
+@functools.lru_cache(maxsize=None)
 def qmla_block_bytes(fmt) -> int:
     return int(_lib.load().qmla_block_bytes(_fmt(fmt)))
 
@@ -149,6 +152,45 @@ def qmla_decode_noalloc(fmt, blocks, block_table, seq_lens, max_seq_len: int, q_
         _p(seq_lens), int(max_seq_len), B, H, _p(q_c), _p(q_r), float(scale), _p(out), _p(lse),
         _p(status), _stream(stream))
     _check("qmla_decode_noalloc", code)
+
+
+@functools.lru_cache(maxsize=64)
+def qmla_decode_step_layout(batch: int, heads: int, n_new: int) -> tuple:
+    """Byte offsets of qmla_decode_step's packed host buffers: (latent, rope_k,
+    q_c, q_r, input bytes, out, lse, output bytes)."""
+    import ctypes
+    o = (ctypes.c_size_t * 8)()
+    _check("qmla_decode_step_layout",
+           _lib.load().qmla_decode_step_layout(int(batch), int(heads), int(n_new), o))
+    return tuple(int(x) for x in o)
+
+
+def qmla_decode_step_workspace_bytes(fmt, batch: int, heads: int, n_new: int,
+                                     max_seq_len: int) -> int:
+    return int(_lib.load().qmla_decode_step_workspace_bytes(
+        _fmt(fmt), int(batch), int(heads), int(n_new), int(max_seq_len)))
+
+
+def qmla_decode_step(fmt, blocks, block_table, seq_lens, max_seq_len: int, heads: int,
+                     n_new: int, h_in, scale: float, h_out, workspace, status,
+                     stream=None) -> None:
+    """One decode step from host memory to host memory: h_in (host uint8, the
+    step's new tokens and queries packed as qmla_decode_step_layout gives) is
+    copied in, the tokens appended and seq_lens advanced, the decode run and
+    out / lse copied into h_out (host uint8); returns once they are there."""
+    B = int(seq_lens.numel())
+    o = qmla_decode_step_layout(B, heads, n_new)
+    if h_in.numel() * h_in.element_size() < o[4] or h_out.numel() * h_out.element_size() < o[7]:
+        raise ValueError("h_in / h_out smaller than qmla_decode_step_layout's sizes")
+    if block_table.shape[0] < B:
+        raise ValueError("block_table has fewer rows than seq_lens")
+    num_blocks = blocks.numel() // qmla_block_bytes(fmt)
+    code = _lib.load().qmla_decode_step(
+        _fmt(fmt), _p(blocks), num_blocks, _p(block_table), int(block_table.shape[1]),
+        _p(seq_lens), int(max_seq_len), B, int(heads), int(n_new), _p(h_in), float(scale),
+        _p(h_out), _p(workspace), int(workspace.numel() * workspace.element_size()), _p(status),
+        _stream(stream))
+    _check("qmla_decode_step", code)
 
 
 def qmla_read_status(status, stream=None) -> int:

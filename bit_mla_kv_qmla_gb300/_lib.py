@@ -15,7 +15,8 @@ _lib = None
 # exported symbols, as declared in include/qmla.h
 SYMBOLS = ("qmla_block_bytes", "qmla_append", "qmla_append_advance",
            "qmla_decode_workspace_bytes", "qmla_decode", "qmla_decode_multi",
-           "qmla_decode_noalloc", "qmla_decode_timeout_test", "qmla_read_status",
+           "qmla_decode_noalloc", "qmla_decode_timeout_test", "qmla_decode_step_layout",
+           "qmla_decode_step_workspace_bytes", "qmla_decode_step", "qmla_read_status",
            "qmla_error_string")
 
 
@@ -49,6 +50,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.qmla_decode_noalloc.restype = ctypes.c_int
     L.qmla_decode_timeout_test.argtypes = L.qmla_decode.argtypes
     L.qmla_decode_timeout_test.restype = ctypes.c_int
+    L.qmla_decode_step_layout.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+    L.qmla_decode_step_layout.restype = ctypes.c_int
+    L.qmla_decode_step_workspace_bytes.argtypes = [ctypes.c_int, i32, i32, i32, i32]
+    L.qmla_decode_step_workspace_bytes.restype = sz
+    L.qmla_decode_step.argtypes = [ctypes.c_int, P, i64, P, i32, P, i32, i32, i32, i32, P, f32, P,
+                                   P, sz, P, P]
+    L.qmla_decode_step.restype = ctypes.c_int
     L.qmla_read_status.argtypes = [P, P]
     L.qmla_read_status.restype = ctypes.c_int
     L.qmla_error_string.argtypes = [ctypes.c_int]

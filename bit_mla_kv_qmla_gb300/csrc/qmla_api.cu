@@ -37,7 +37,7 @@ int max_slots(int batch, int heads, int sms) {
 int append_impl(int format, void* blocks, int64_t num_blocks, const int32_t* block_table,
                 int32_t max_blocks_per_seq, int32_t* positions, int32_t batch, int32_t n_new,
                 const void* latent, const void* rope_k, int32_t* status_dev, void* stream,
-                bool advance) {
+                bool advance, bool launch = true) {
   if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
   if (batch < 0 || n_new < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
     return QMLA_ERR_INVALID_ARG;
@@ -49,6 +49,7 @@ int append_impl(int format, void* blocks, int64_t num_blocks, const int32_t* blo
       !aligned(block_table, 4) || !aligned(positions, 4) || !aligned(status_dev, 4))
     return QMLA_ERR_INVALID_ARG;
   if (max_blocks_per_seq == 0) return QMLA_ERR_INVALID_ARG;
+  if (!launch) return QMLA_OK;
   cudaError_t e = qmla::launch_append(
       format, static_cast<uint8_t*>(blocks), num_blocks, block_table, max_blocks_per_seq,
       positions, batch, n_new, static_cast<const __nv_bfloat16*>(latent),
@@ -62,7 +63,8 @@ int decode_impl(int format, const void* blocks, int64_t num_blocks, const int32_
                 int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
                 int32_t batch, int32_t heads, int32_t q_len, int32_t q_heads, const void* q_c,
                 const void* q_r, float softmax_scale, void* out, float* lse, void* workspace,
-                size_t workspace_bytes, int32_t* status_dev, void* stream, int withhold = 0) {
+                size_t workspace_bytes, int32_t* status_dev, void* stream, int withhold = 0,
+                bool launch = true) {
   if (!known_format(format)) return QMLA_ERR_UNSUPPORTED;
   if (batch < 0 || max_seq_len < 0 || max_blocks_per_seq < 0 || num_blocks < 1)
     return QMLA_ERR_INVALID_ARG;
@@ -80,6 +82,7 @@ int decode_impl(int format, const void* blocks, int64_t num_blocks, const int32_
   if (sms <= 0) return QMLA_ERR_CUDA;
   const int slots = max_slots(batch, heads, sms);
   if (workspace_bytes < qmla::workspace_bytes(batch, heads, slots)) return QMLA_ERR_WORKSPACE;
+  if (!launch) return QMLA_OK;
 
   qmla::DecodeArgs a;
   a.fmt = format;
@@ -114,6 +117,28 @@ int decode_impl(int format, const void* blocks, int64_t num_blocks, const int32_
   if (e != cudaSuccess) return QMLA_ERR_CUDA;
   e = qmla::launch_combine(a.ws, batch, heads, static_cast<__nv_bfloat16*>(out), lse, s);
   return e == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
+}
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Offsets of qmla_decode_step's packed host buffers (qmla.h).
+void step_layout(int32_t batch, int32_t heads, int32_t n_new, size_t* o) {
+  const size_t B = size_t(batch), H = size_t(heads), n = size_t(n_new);
+  size_t off = 0;
+  o[0] = o[1] = 0;
+  if (n_new > 0) {
+    o[0] = off;
+    off = up256(off + B * n * QMLA_D_C * 2);
+    o[1] = off;
+    off = up256(off + B * n * QMLA_D_R * 2);
+  }
+  o[2] = off;
+  off = up256(off + B * H * QMLA_D_C * 2);
+  o[3] = off;
+  o[4] = off + B * H * QMLA_D_R * 2;
+  o[5] = 0;
+  o[6] = up256(B * H * QMLA_D_C * 2);
+  o[7] = o[6] + B * H * 4;
 }
 
 }  // namespace
@@ -197,6 +222,72 @@ int qmla_decode_timeout_test(int format, const void* blocks, int64_t num_blocks,
   return decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
                      max_seq_len, batch, heads, 1, 0, q_c, q_r, softmax_scale, out, lse,
                      workspace, workspace_bytes, status_dev, stream, 1);
+}
+
+int qmla_decode_step_layout(int32_t batch, int32_t heads, int32_t n_new, size_t* offsets) {
+  if (!offsets || batch < 0 || heads < 0 || n_new < 0) return QMLA_ERR_INVALID_ARG;
+  step_layout(batch, heads, n_new, offsets);
+  return QMLA_OK;
+}
+
+size_t qmla_decode_step_workspace_bytes(int format, int32_t batch, int32_t heads, int32_t n_new,
+                                        int32_t max_seq_len) {
+  if (n_new < 0) return 0;
+  const size_t dws = qmla_decode_workspace_bytes(format, batch, heads, max_seq_len);
+  if (dws == 0) return 0;
+  size_t o[8];
+  step_layout(batch, heads, n_new, o);
+  return up256(o[4]) + up256(o[7]) + dws;
+}
+
+int qmla_decode_step(int format, void* blocks, int64_t num_blocks, const int32_t* block_table,
+                     int32_t max_blocks_per_seq, int32_t* seq_lens, int32_t max_seq_len,
+                     int32_t batch, int32_t heads, int32_t n_new, const void* h_in,
+                     float softmax_scale, void* h_out, void* workspace, size_t workspace_bytes,
+                     int32_t* status_dev, void* stream) {
+  if (batch < 0 || heads < 0 || n_new < 0) return QMLA_ERR_INVALID_ARG;
+  if (!h_in || !h_out || !workspace) return QMLA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return QMLA_ERR_INVALID_ARG;
+  const size_t need = qmla_decode_step_workspace_bytes(format, batch, heads, n_new, max_seq_len);
+  if (need == 0) {
+    if (!known_format(format) || !heads_served(format, heads)) return QMLA_ERR_UNSUPPORTED;
+    return max_seq_len < 0 ? QMLA_ERR_INVALID_ARG : QMLA_ERR_CUDA;
+  }
+  if (workspace_bytes < need) return QMLA_ERR_WORKSPACE;
+  if (batch == 0) return QMLA_OK;
+  size_t o[8];
+  step_layout(batch, heads, n_new, o);
+  uint8_t* d_in = static_cast<uint8_t*>(workspace);
+  uint8_t* d_out = d_in + up256(o[4]);
+  uint8_t* d_ws = d_out + up256(o[7]);
+  const size_t dws = need - up256(o[4]) - up256(o[7]);
+  // every argument checked before anything is enqueued
+  int r = n_new > 0 ? append_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq,
+                                  seq_lens, batch, n_new, d_in + o[0], d_in + o[1], status_dev,
+                                  stream, true, false)
+                    : QMLA_OK;
+  if (r != QMLA_OK) return r;
+  r = decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
+                  max_seq_len, batch, heads, 1, 0, d_in + o[2], d_in + o[3], softmax_scale,
+                  d_out + o[5], reinterpret_cast<float*>(d_out + o[6]), d_ws, dws, status_dev,
+                  stream, 0, false);
+  if (r != QMLA_OK) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(d_in, h_in, o[4], cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return QMLA_ERR_CUDA;
+  if (n_new > 0) {
+    r = append_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens, batch,
+                    n_new, d_in + o[0], d_in + o[1], status_dev, stream, true);
+    if (r != QMLA_OK) return r;
+  }
+  r = decode_impl(format, blocks, num_blocks, block_table, max_blocks_per_seq, seq_lens,
+                  max_seq_len, batch, heads, 1, 0, d_in + o[2], d_in + o[3], softmax_scale,
+                  d_out + o[5], reinterpret_cast<float*>(d_out + o[6]), d_ws, dws, status_dev,
+                  stream);
+  if (r != QMLA_OK) return r;
+  if (cudaMemcpyAsync(h_out, d_out, o[7], cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return QMLA_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? QMLA_OK : QMLA_ERR_CUDA;
 }
 
 int qmla_read_status(const int32_t* status_dev, void* stream) {

@@ -288,6 +288,54 @@ int qmla_decode_timeout_test(int format, const void* blocks, int64_t num_blocks,
                              float softmax_scale, void* out, float* lse, void* workspace,
                              size_t workspace_bytes, int32_t* status_dev, void* stream);
 
+/* qmla_decode_step_layout - byte offsets of the packed host buffers of
+ * qmla_decode_step.  Regions follow one another, each starting at the first
+ * multiple of 256 bytes at or after the end of the one before (the first at
+ * 0):
+ *   input   latent [batch][n_new][512] bf16, rope_k [batch][n_new][64] bf16,
+ *           q_c [batch][heads][512] bf16, q_r [batch][heads][64] bf16
+ *           (n_new = 0: only q_c and q_r; their offsets are then 0 and
+ *           after q_c, and the latent and rope_k entries are 0)
+ *   output  out [batch][heads][512] bf16, lse [batch][heads] float32
+ * offsets[0..7] = latent, rope_k, q_c, q_r, input bytes (the end of q_r),
+ * out, lse, output bytes (the end of lse).  Returns QMLA_OK, or INVALID_ARG
+ * for a null `offsets` or negative sizes.  Host-only arithmetic. */
+int qmla_decode_step_layout(int32_t batch, int32_t heads, int32_t n_new, size_t* offsets);
+
+/* Device workspace bytes qmla_decode_step needs: staging of one step's
+ * input and output buffers plus qmla_decode's workspace; 0 for unsupported
+ * arguments. */
+size_t qmla_decode_step_workspace_bytes(int format, int32_t batch, int32_t heads,
+                                        int32_t n_new, int32_t max_seq_len);
+
+/* qmla_decode_step - one decode step of a serving loop, from host memory to
+ * host memory, in one call: the step's input buffer (n_new new tokens per
+ * sequence, n_new >= 0, and the queries; layout of qmla_decode_step_layout)
+ * is copied to the device, the tokens are appended and every length advanced
+ * by n_new (qmla_append_advance), the decode runs over the advanced lengths
+ * (qmla_decode), out and lse are copied into the output buffer, and the call
+ * returns once they are there (it synchronizes `stream`).  The pages' decode
+ * step (append the new token's compressed latent, attend over the cache);
+ * the packing of host buffers is this library's.
+ *   h_in          host, >= offsets[4] bytes, read
+ *   h_out         host, >= offsets[7] bytes, written
+ *   seq_lens      [batch] int32 device: lengths before the step, advanced
+ *   max_seq_len   bound on the advanced lengths
+ *   workspace     device, >= qmla_decode_step_workspace_bytes(...) bytes,
+ *                 256-byte aligned; contents need no initialization
+ * Other arguments as for qmla_append_advance and qmla_decode.  Page-locked
+ * host buffers (cudaHostAlloc) let the copies run asynchronously at full
+ * speed; pageable ones work too.  Errors: those of qmla_append_advance and
+ * qmla_decode, checked before anything is enqueued; CUDA when a copy, a
+ * launch or the synchronization fails (work before the failing step may
+ * then have run).  Device status bits as for those calls. */
+int qmla_decode_step(int format, void* blocks, int64_t num_blocks,
+                     const int32_t* block_table, int32_t max_blocks_per_seq,
+                     int32_t* seq_lens, int32_t max_seq_len, int32_t batch, int32_t heads,
+                     int32_t n_new, const void* h_in, float softmax_scale, void* h_out,
+                     void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                     void* stream);
+
 /* Synchronize `stream`, read *status_dev and return QMLA_OK if it is 0,
  * QMLA_ERR_DEVICE otherwise (QMLA_ERR_CUDA if the copy failed). */
 int qmla_read_status(const int32_t* status_dev, void* stream);

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     assert names == sorted(["qmla_block_bytes", "qmla_append", "qmla_append_advance",
                             "qmla_decode_workspace_bytes", "qmla_decode_multi",
                             "qmla_decode", "qmla_decode_noalloc", "qmla_decode_timeout_test",
-                            "qmla_read_status", "qmla_error_string"])
+                            "qmla_decode_step_layout", "qmla_decode_step_workspace_bytes",
+                            "qmla_decode_step", "qmla_read_status", "qmla_error_string"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -145,6 +146,60 @@ def test_decode_noalloc_rejects_bad_arguments(lib):
     # the formats qmla_decode serves are accepted up to the device query
     for fmt in (0, 1, 2, 3, 4):
         assert call(fmt=fmt, batch=0) == 0
+
+
+def _step_offsets_by_rule(batch, heads, n_new):
+    # the packing rule stated in qmla.h: regions in order, each at the first
+    # multiple of 256 at or after the end of the previous one
+    def up(x):
+        return -(-x // 256) * 256
+    sizes_in = ([batch * n_new * 512 * 2, batch * n_new * 64 * 2] if n_new else []) + \
+        [batch * heads * 512 * 2, batch * heads * 64 * 2]
+    offs, end = [], 0
+    for n in sizes_in:
+        offs.append(up(end))
+        end = offs[-1] + n
+    lat, rope = (offs[0], offs[1]) if n_new else (0, 0)
+    qc, qr = offs[-2], offs[-1]
+    out, lse = 0, up(batch * heads * 512 * 2)
+    return (lat, rope, qc, qr, end, out, lse, lse + batch * heads * 4)
+
+
+@pytest.mark.parametrize("batch,heads,n_new", [(4, 128, 1), (32, 16, 1), (3, 16, 0), (1, 128, 5),
+                                                (7, 48, 3), (0, 16, 1)])
+def test_decode_step_layout_follows_the_stated_rule(lib, batch, heads, n_new):
+    o = (ctypes.c_size_t * 8)()
+    assert lib.qmla_decode_step_layout(batch, heads, n_new, o) == 0
+    assert tuple(o) == _step_offsets_by_rule(batch, heads, n_new)
+
+
+def test_decode_step_layout_rejects_bad_arguments(lib):
+    o = (ctypes.c_size_t * 8)()
+    assert lib.qmla_decode_step_layout(-1, 16, 1, o) == -1
+    assert lib.qmla_decode_step_layout(1, -16, 1, o) == -1
+    assert lib.qmla_decode_step_layout(1, 16, -1, o) == -1
+    assert lib.qmla_decode_step_layout(1, 16, 1, None) == -1
+
+
+def test_decode_step_rejects_bad_arguments(lib):
+    # every rejection below returns before the library touches the device
+    keep, p = _fake(4096)
+
+    def call(fmt=0, heads=128, batch=1, n_new=1, h_in=p, h_out=p, ws=p, msl=256):
+        return lib.qmla_decode_step(fmt, p, 4, p, 4, p, msl, batch, heads, n_new, h_in,
+                                    ctypes.c_float(0.1), h_out, ws, 1 << 20, p, None)
+    assert call(batch=-1) == -1
+    assert call(heads=-16) == -1
+    assert call(n_new=-1) == -1
+    assert call(h_in=None) == -1
+    assert call(h_out=None) == -1
+    assert call(ws=None) == -1
+    assert call(ws=p + 128) == -1     # workspace must be 256-byte aligned
+    assert call(fmt=5) == -2
+    assert call(heads=17) == -2
+    assert call(msl=-1) == -1
+    assert lib.qmla_decode_step_workspace_bytes(0, 1, 16, -1, 256) == 0
+    assert lib.qmla_decode_step_workspace_bytes(5, 1, 16, 1, 256) == 0
 
 
 def test_host_plan_restatement_covers_every_block_once():
