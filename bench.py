@@ -200,6 +200,13 @@ def step_launches(w, n_app, tc):
     return k
 
 
+# The error tables are measured with the library's quantizer: every group's
+# scale and zero on its binary16-exact grid (z = Z*2^E, s = M*2^E, integers
+# Z and Z + levels*M within +-2047), codes rounded half to even.
+QUANTIZER_NOTE = ("binary16-exact grid per 64-channel group: z = Z*2^E, s = M*2^E "
+                  "(|Z|, |Z + levels*M| <= 2047), codes round-half-even")
+
+
 def append_per_step(cfg, w):
     """Tokens appended per sequence per step: one for the serving steps
     (configurations 1 and 4), the workload's own count otherwise."""
@@ -475,6 +482,7 @@ def measure_fold(device):
         if row:
             res[fmt] = row
     torch.cuda.empty_cache()
+    res["quantizer"] = QUANTIZER_NOTE
     return {"folded_rotation_error_b8_h16_l2048_x10pct1": res}
 
 
@@ -538,6 +546,7 @@ def measure_rope_bits(device):
         del cache
     torch.cuda.empty_cache()
     return {"rope_bits_ablation_h16_x10pct1": {
+        "quantizer": QUANTIZER_NOTE,
         "bytes_per_token": {f: qmla_block_bytes(f) // 64 for f in fmts},
         "score_rms_bf16_l1_b4096": score_rms,
         "score_rms_error_l1_b4096": score_err,
