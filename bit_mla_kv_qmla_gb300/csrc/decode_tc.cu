@@ -144,13 +144,16 @@ constexpr int kMmaWarp = 0;
 constexpr int kXchgWarp = 1;   // moves this CTA's P rows to the peer
 constexpr int kSmxWarp0 = 4;   // 8 softmax warps (warpgroups 1-2)
 constexpr int kDqWarp0 = 12;   // 8 dequantization warps (warpgroups 3-4)
-// registers per thread of the issuer warpgroup, the softmax and the
-// dequantization warps; the BF16 rows need no codes held ahead of use
+// registers per thread at launch (__launch_bounds__ at 20 warps; the
+// launcher checks the compiled kernel's count) and of the issuer warpgroup,
+// the softmax and the dequantization warps after setmaxnreg; the BF16 rows
+// need no codes held ahead of use
+constexpr uint32_t kRegsLaunch = 96;
 template <int kCBits>
 struct RegSplit {
   static constexpr uint32_t idle = kCBits == 16 ? 64 : 48, smx = 104, dq = kCBits == 16 ? 104 : 112;
-  static_assert(128 * idle + 256 * smx + 256 * dq <= kThreads * 96,
-                "register split within the launch allocation (96 per thread at 20 warps)");
+  static_assert(128 * idle + 256 * smx + 256 * dq <= kThreads * kRegsLaunch,
+                "register split within the launch allocation");
 };
 
 // tensor memory (32-bit columns)
@@ -435,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp < kSmxWarp0) {
     // the first warpgroup (all four warps at this one instruction) gives up
     // registers; only its first warp has work
-    setmaxnreg_dec<RegSplit<kCBits>::idle>();
+    setmaxnreg_to<kRegsLaunch, RegSplit<kCBits>::idle>();
   }
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -575,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // idle warps of the first warpgroup
   } else if (warp < kDqWarp0) {
     // ------------------------------------------------------------ softmax
-    setmaxnreg_inc<RegSplit<kCBits>::smx>();
+    setmaxnreg_to<kRegsLaunch, RegSplit<kCBits>::smx>();
     // thread = token row tt of S^T (its lane quarter's tensor-memory lanes);
     // the warp holds 32 of this CTA's 64 heads.  For O (lane = head) the same
     // thread stands for head tt.
@@ -836,7 +839,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant
-    setmaxnreg_inc<RegSplit<kCBits>::dq>();
+    setmaxnreg_to<kRegsLaunch, RegSplit<kCBits>::dq>();
     // thread = token row tt of the tile (tensor-memory lane); rows 0-63 come
     // from the tile's first block, 64-127 from its second.  Units per tile:
     //   dh 0: A (tensor memory) the other half's chunks 0, 1, 2;
@@ -1106,7 +1109,8 @@ cudaError_t launch_decode_tc128(const DecodeArgs& a, cudaStream_t stream) {
                 : a.fmt == QMLA_C2R4 ? decode_tc128_kernel<2>
                                      : decode_tc128_kernel<16>;
   e = ensure_smem_attr(kernel, int(kSmDyn),
-                       a.fmt == QMLA_C4R4 ? done4 : a.fmt == QMLA_C2R4 ? done2 : done16);
+                       a.fmt == QMLA_C4R4 ? done4 : a.fmt == QMLA_C2R4 ? done2 : done16,
+                       int(kRegsLaunch));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(2 * a.workers));

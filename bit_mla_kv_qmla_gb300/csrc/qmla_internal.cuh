@@ -140,12 +140,23 @@ struct DecodeArgs {
 // attribute is per function and device; repeating it costs a runtime call on
 // every launch).  `done` is the caller's own per-device record for this kernel.
 constexpr int kMaxDevices = 64;
+// regs > 0: the kernel hands registers between warpgroups with setmaxnreg
+// on the assumption that it launches with `regs` per thread; a build that
+// compiled it to another count is refused here (its register increases
+// would wait on registers nobody released) instead of launched.
 template <typename K>
-inline cudaError_t ensure_smem_attr(K* kernel, int bytes, int (&done)[kMaxDevices]) {
+inline cudaError_t ensure_smem_attr(K* kernel, int bytes, int (&done)[kMaxDevices],
+                                    int regs = 0) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDevices && done[dev] >= bytes) return cudaSuccess;
+  if (regs > 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != regs) return cudaErrorInvalidDeviceFunction;
+  }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = bytes;
   return e;

@@ -225,6 +225,16 @@ template <uint32_t kRegs>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
+// From kFrom registers per thread (the launch's count) to kTo: an increase
+// or a decrease as the two compare (an increase may only raise the count, a
+// decrease only lower it); nothing when they are equal.
+template <uint32_t kFrom, uint32_t kTo>
+__device__ __forceinline__ void setmaxnreg_to() {
+  if constexpr (kTo > kFrom)
+    setmaxnreg_inc<kTo>();
+  else if constexpr (kTo < kFrom)
+    setmaxnreg_dec<kTo>();
+}
 
 // ---------------------------------------------------------------- TMEM
 // Warp-wide: allocate `ncols` (power of two >= 32) columns, address -> *dst.
