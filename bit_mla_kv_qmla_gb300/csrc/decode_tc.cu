@@ -1100,9 +1100,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 cudaError_t launch_decode_tc128(const DecodeArgs& a, cudaStream_t stream) {
   static int done4[kMaxDevices], done2[kMaxDevices], done16[kMaxDevices];
   DecodeArgs b = a;
-  // A second piece costs a worker about one tile (the queries' staging and
-  // the epilogue); the split charges it two blocks.
-  b.piece_cost = 2;
+  // A second piece costs a worker about three tiles (the pipeline's drain
+  // and refill, the epilogue, the queries' staging; measured by the charge
+  // that makes the 64-sequence ragged workload fastest); the split charges
+  // it six blocks.
+  b.piece_cost = 6;
   cudaError_t e = launch_plan(b, stream);
   if (e != cudaSuccess) return e;
   auto kernel = a.fmt == QMLA_C4R4   ? decode_tc128_kernel<4>

@@ -210,7 +210,7 @@ def test_host_plan_restatement_covers_every_block_once():
     import random
     from helpers import boundary_sequences, plan_pieces
     rng = random.Random(5)
-    for workers, cost in ((76, 2), (152, 3), (7, 0)):
+    for workers, cost in ((76, 6), (76, 2), (152, 3), (7, 0)):
         nb = [rng.choice([0, 1, 2, 5, 64, 300]) for _ in range(50)]
         plan = plan_pieces(nb, workers, cost)
         seen = []

@@ -16,6 +16,10 @@ from bit_mla_kv_qmla_gb300.cache import Decoder, PagedCache, build_cache
 from helpers import boundary_sequences, compare_rows, oracle_pool_for_seq, sample_heads
 
 pytestmark = pytest.mark.gpu
+
+# blocks the 128-head kernel's split charges for each sequence a worker
+# starts (decode_tc.cu, launch_decode_tc128)
+TC128_PIECE_COST = 6
 FMTS = ["C4R4", "C2R4", "BF16", "C4R2", "C2R2"]
 
 
@@ -124,8 +128,8 @@ def test_decode_full_size_sampled(cfg, fmt, seqs, nheads):
     if seqs is None:
         assert w.heads == 128
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        # the 128-head kernel: one worker per CTA pair, two blocks of piece cost
-        seqs = boundary_sequences([(L + 63) // 64 for L in lens], sms // 2, 2)
+        # the 128-head kernel: one worker per CTA pair, six blocks of piece cost
+        seqs = boundary_sequences([(L + 63) // 64 for L in lens], sms // 2, TC128_PIECE_COST)
     cache = build_cache(w, "cuda", gen_device="cuda")
     qc, qr = W.queries(w, device="cuda")
     out, lse = Decoder(cache, w.heads, max(lens))(qc, qr, w.scale)
@@ -312,7 +316,7 @@ def test_plan_matches_host_restatement():
     seq_table = ws[:B * 8].view(torch.int32).view(B, 2)
     off = a256(B * 8) + a256(slots * H * 4) + a256(slots * H * 512 * 4)
     pieces = ws[off:off + slots * 16].view(torch.int32).view(slots, 4)
-    want = plan_pieces([(L + 63) // 64 for L in lens], sms // 2, 2)
+    want = plan_pieces([(L + 63) // 64 for L in lens], sms // 2, TC128_PIECE_COST)
     for b in range(B):
         base, n = seq_table[b].tolist()
         assert n == len(want[b]), b
