@@ -51,7 +51,7 @@ def _unpack(o, h_out, batch, heads):
     ("C4R4", 16, [0, 4000, 63, 64, 65], 3),
 ])
 def test_host_step_matches_device_calls_and_oracle(fmt, heads, lens, n_new):
-    steps = 2
+    steps = 3
     w = _workload(fmt, heads, lens, 41)
     caches = [build_cache(w, "cuda", lens=lens, extra_tokens=steps * n_new, gen_device="cpu")
               for _ in range(2)]
