@@ -654,12 +654,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 32; ++h) d[h] = -INFINITY;
           } else if (a.q_heads > 0) {
-            // multi-token query: the last q_len - 1 positions are not visible to every row
-            const int pos = j * kT + (tt & 63);
-            if (pos >= L - a.q_len + 1) {
+            // multi-token query: the last q_len - 1 positions are not visible to
+            // every row.  Virtual head v (query v / q_heads) sees positions up to
+            // L - q_len + v / q_heads, so position pos = L - q_len + 1 + e is
+            // hidden from v exactly when v < (e + 1) q_heads: a prefix of this
+            // thread's heads, found without a division per head.
+            const int e = j * kT + (tt & 63) - (L - a.q_len + 1);
+            if (e >= 0) {
+              const int hcut = (e + 1) * a.q_heads - (64 * int(rank) + 32 * hh);
 #pragma unroll
               for (int h = 0; h < 32; ++h)
-                if (pos >= visible_tokens(a, 64 * int(rank) + 32 * hh + h, L)) d[h] = -INFINITY;
+                if (h < hcut) d[h] = -INFINITY;
             }
           }
         };
