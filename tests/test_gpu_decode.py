@@ -281,6 +281,30 @@ def test_decode_plan_source_boundary(batch):
         compare_rows(out[b:b + 1], lse[b:b + 1], o, l, f"batch {batch} seq {b}")
 
 
+@pytest.mark.parametrize("fmt,heads", [("C4R4", 16), ("C2R4", 16), ("C4R4", 128)])
+def test_decode_one_long_sequence(fmt, heads):
+    """One 131072-token sequence: the split gives every worker a piece of it
+    (152 pieces at 16 heads, 76 at 128), the most partials the merge ever
+    combines for one sequence (in rounds of eight).  Sampled heads against
+    the oracle, plus an empty second sequence whose row must be O = 0,
+    LSE = -inf."""
+    w = W.Workload(f"long_{fmt}_{heads}", fmt, 2, heads, 131072, 0, "x10pct1", 0, 53)
+    lens = [131072, 0]
+    cache = build_cache(w, "cuda", lens=lens, gen_device="cuda")
+    qc, qr = W.queries(w, device="cuda")
+    out, lse = Decoder(cache, heads, max(lens))(qc, qr, w.scale)
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0
+    table = cache.block_table.cpu().numpy()
+    hs = sample_heads(heads, 4, 61)
+    pool = oracle_pool_for_seq(w, 0, lens[0], table[0], cache.num_blocks, "cuda")
+    ro, rl = oracle.decode(W.FORMATS[fmt], pool, table[0:1], np.array([lens[0]]),
+                           qc[0:1, hs].cpu(), qr[0:1, hs].cpu(), w.scale)
+    compare_rows(out[0, hs], lse[0, hs], ro[0], rl[0], w.name)
+    assert torch.count_nonzero(out[1]).item() == 0
+    assert torch.isneginf(lse[1]).all()
+
+
 def test_decode_max_heads():
     """256 query heads, the most any kernel serves (the CUDA-core kernel)."""
     w = W.Workload("heads256", "C4R4", 2, 256, 300, 0, "lognormal8", 0, 47)
