@@ -31,10 +31,10 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // ---------------------------------------------------------------- mbarrier
-// A waiting thread is suspended by the hardware for up to this long per
-// try_wait (it resumes as soon as the phase completes), so waiting warps do
-// not take issue slots from working ones.
-constexpr uint32_t kSuspendNs = 20000;
+// try_wait may suspend a waiting thread for a time the hardware chooses (it
+// resumes when the phase completes), so waiting warps take few issue slots
+// from working ones.  No suspend-time hint is given: with a hint of 20 us the
+// 16-head decode measured 1.5 % slower and the ragged 128-head one 2.6 %.
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }
@@ -58,10 +58,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -71,10 +71,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
